@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed fused-MoE expert GEMM on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic routed
+input already resident in HBM: the dispatch tables built on the GPU from
+topk_ids (moe_build_dispatch), then phase 1 + phase 2 (moe_fused_forward).
+
+Metric: fused MoE forward TFLOP/s over valid rows, 2·pairs·3·hidden·intermediate
+per step ÷ step time.  Default workload: DeepSeek-V2-Lite-shaped (4096 tokens,
+top-6 of 64 experts, hidden 2048, intermediate 1408, uniform routing); its
+working set (1.45 GB) is far larger than the 129 MB L2, so back-to-back steps
+do not reuse L2 between iterations.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the reference arm for this build: the pages' own kernel targets a
+MetaX C500 and cannot run here).
+
+Multi-GPU: the path does not shard inside one forward on one GPU; N ranks run
+independent replicas of the workload ("replicas only"), value = units of all
+ranks ÷ the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused MoE forward TFLOP/s (valid rows) and % of roofline on 1 GB300"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="dsv2_lite")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample (cpu_baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, profiles
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.t_begin = None
+        self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark_begin(self):
+        self.t_begin = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for t, r in self.rows if self.t_begin and self.t_end and self.t_begin <= t <= self.t_end]
+        used = inside if inside else [r for _, r in self.rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, pw = [], [], []
+        for r in used:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(used),
+                "samples_in_timed_region": len(inside)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("routed_grouped_gemm_dispatch_gb300/csrc/grouped_gemm.cu",
+                "routed_grouped_gemm_dispatch_gb300/csrc/sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per phase-1 launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"phase1_gate_up_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# workload preparation
+# ---------------------------------------------------------------------------
+
+def prepare_device(w, seed, dev):
+    """Routing, tokens and expert weights; GPU tables and packing."""
+    import torch
+
+    import routed_grouped_gemm_dispatch_gb300 as moe
+    import workloads
+
+    ids_np, tw_np = workloads.routing(w, seed)
+    x_np = workloads.tokens(w, seed)
+    gate, up, down = workloads.expert_weights(w, seed, device=str(dev))
+    T, k = ids_np.shape
+    ids = torch.from_numpy(ids_np).to(dev)
+    tables = moe.build_dispatch(ids, w.experts)
+    flat = ids.reshape(-1).long()
+    P = flat.numel()
+    order = torch.sort(flat, stable=True).indices
+    e_sorted = flat[order]
+    rank = torch.arange(P, device=dev) - tables["group_offsets"].long()[e_sorted]
+    rows = torch.empty(P, dtype=torch.long, device=dev)
+    rows[order] = tables["group_padded_offsets"].long()[e_sorted] + rank
+    rows_total = tables["group_idx_for_bx"].numel() * moe.BLOCK_TOKEN
+    xp = torch.full((rows_total, w.hidden), float("nan"), dtype=torch.float16, device=dev)
+    xp[rows] = torch.from_numpy(x_np).to(dev)[torch.arange(P, device=dev) // k]
+    rw = torch.from_numpy(tw_np).to(dev).reshape(-1)[order].contiguous()
+    ul = torch.zeros((rows_total, w.intermediate), dtype=torch.float16, device=dev)
+    out = torch.zeros((rows_total, w.hidden), dtype=torch.float16, device=dev)
+    torch.cuda.synchronize(dev)
+    return dict(ids=ids, tables=tables, xp=xp, rw=rw, ul=ul, out=out, gate=gate, up=up, down=down,
+                ids_np=ids_np, tw_np=tw_np, x_np=x_np, rows_total=rows_total, pair_rows=rows)
+
+
+def touched_bytes(w, sizes):
+    import numpy as np
+    touched = int(np.count_nonzero(sizes))
+    wbytes = 6.0 * w.hidden * w.intermediate * touched
+    P = w.pairs
+    act = P * (2.0 * w.hidden + 2.0 * w.hidden + 4.0 + 4.0 * w.intermediate)
+    return wbytes, act, touched
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, seed, target_s, host=None):
+    """Time the CPU oracle on a bounded sample of valid rows of the workload.
+    Returns (TFLOP/s, sample description, threads, seconds)."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    if host is None:
+        ids_np, tw_np = workloads.routing(w, seed)
+        x_np = workloads.tokens(w, seed)
+        g, u, d = workloads.expert_weights(w, seed, device="cpu")
+        host = dict(ids_np=ids_np, tw_np=tw_np, x_np=x_np, g=g.numpy(), u=u.numpy(), d=d.numpy())
+    tab = oracle.build_dispatch(host["ids_np"], w.experts)
+    prow = oracle.pair_padded_rows(host["ids_np"], w.experts, tab["group_padded_offsets"])
+    rows_total = tab["num_blocks_m"] * oracle.BLOCK_TOKEN
+    xo, rwo = oracle.pack(host["x_np"], host["ids_np"], host["tw_np"], prow, tab, rows_total)
+    threads = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(seed)
+    valid = prow.reshape(-1)
+    per_row_flops = 6.0 * w.hidden * w.intermediate
+
+    def run(n):
+        rows = rng.choice(valid, size=n, replace=False)
+        t0 = time.perf_counter()
+        oracle.forward_rows(xo, host["g"], host["u"], host["d"], rwo, tab, rows, n_threads=threads)
+        return time.perf_counter() - t0
+
+    n0 = min(valid.size, max(threads, 8))
+    t0 = run(n0)
+    n = int(min(valid.size, max(n0, round(n0 * target_s / max(t0, 1e-6)))))
+    dt = run(n)
+    rate = n * per_row_flops / dt / 1e12
+    desc = (f"{n} randomly chosen valid rows of {valid.size} (each row's full phase 1 and "
+            f"phase 2, fp32 accumulation), {threads} OpenMP threads")
+    return rate, desc, threads, dt, host, (xo, rwo, tab, valid)
+
+
+def reference_arm(args, w):
+    import numpy as np
+
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    # size each step so that warmup + steps finish within ~3 minutes
+    budget = 180.0 / max(1, args.steps + args.warmup)
+    per_step_target = max(0.2, min(3.0, budget))
+    rate0, _, threads, _, host, (xo, rwo, tab, valid) = oracle_sample_rate(w, args.seed, per_step_target)
+    per_row = 6.0 * w.hidden * w.intermediate
+    n = max(1, int(rate0 * 1e12 * per_step_target / per_row))
+    n = min(n, valid.size)
+    rng = np.random.default_rng(args.seed + 1)
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = rng.choice(valid, size=n, replace=False)
+        t0 = time.perf_counter()
+        oracle.forward_rows(xo, host["g"], host["u"], host["d"], rwo, tab, rows, n_threads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n * per_row / (ms / 1e3) / 1e12
+    sample = (f"per step {n} randomly chosen valid rows of {valid.size} (each row's full phase 1 "
+              f"and phase 2), {threads} OpenMP threads")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_of(w, "host cores; bounded sample per step"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, l2):
+    return {"workload": w.name, "tokens": w.tokens, "top_k": w.top_k, "experts": w.experts,
+            "hidden": w.hidden, "intermediate": w.intermediate, "pairs": w.pairs,
+            "routing": w.routing + (f"(s={w.zipf_s})" if w.routing == "zipf" else ""),
+            "block_token": 128, "l2": l2}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    import workloads
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+        return
+
+    import numpy as np
+    import torch
+
+    import routed_grouped_gemm_dispatch_gb300 as moe
+    moe.lib()  # fail loudly if the library is missing
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    d = prepare_device(w, args.seed + rank, dev)
+    t = d["tables"]
+    E = w.experts
+
+    def step():
+        moe.build_dispatch(d["ids"], E, out=t)
+        moe.fused_forward(d["xp"], d["gate"], d["up"], d["down"], d["rw"], t["group_sizes"],
+                          t["group_offsets"], t["group_padded_offsets"], t["group_idx_for_bx"],
+                          d["ul"], d["out"])
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark_begin()
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize(dev)
+    sampler.mark_end()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    sampler.stop()
+    flops = w.flops()
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # ---- per-phase durations (same stream, CUDA events) -------------------
+    n_ph = max(5, min(args.steps, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ph)]
+    for i in range(n_ph):
+        e = evs[i]
+        e[0].record()
+        moe.build_dispatch(d["ids"], E, out=t)
+        e[1].record()
+        moe.fused_forward(d["xp"], d["gate"], d["up"], d["down"], d["rw"], t["group_sizes"],
+                          t["group_offsets"], t["group_padded_offsets"], t["group_idx_for_bx"],
+                          d["ul"], d["out"], status=status, flags=moe.MOE_RUN_PHASE1)
+        e[2].record()
+        moe.fused_forward(d["xp"], d["gate"], d["up"], d["down"], d["rw"], t["group_sizes"],
+                          t["group_offsets"], t["group_padded_offsets"], t["group_idx_for_bx"],
+                          d["ul"], d["out"], status=status, flags=moe.MOE_RUN_PHASE2 | moe.MOE_NO_PDL)
+        e[3].record()
+    torch.cuda.synchronize(dev)
+    dispatch_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    p1_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    p2_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    dev_status = int(status.item())
+
+    # ---- end to end through the public API with host buffers ---------------
+    e2e = None
+    if not args.no_e2e:
+        h_ids = d["ids"].cpu().pin_memory()
+        h_x = d["xp"].cpu().pin_memory()
+        h_rw = d["rw"].cpu().pin_memory()
+        h_out = torch.empty_like(d["out"], device="cpu").pin_memory()
+        n_e2e = max(5, min(args.steps, 100))
+
+        def e2e_step():
+            d["ids"].copy_(h_ids, non_blocking=True)
+            d["xp"].copy_(h_x, non_blocking=True)
+            d["rw"].copy_(h_rw, non_blocking=True)
+            step()
+            h_out.copy_(d["out"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        h2d = h_ids.numel() * 4 + h_x.numel() * 2 + h_rw.numel() * 4
+        d2h = h_out.numel() * 2
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": n_e2e,
+               "path": "pinned host topk_ids + stacked tokens + routed weights -> H2D -> "
+                       "moe_build_dispatch -> moe_fused_forward -> D2H out"}
+
+    # ---- roofline --------------------------------------------------------------
+    peaks, src = load_peaks()
+    sizes = t["group_sizes"].cpu().numpy()
+    wbytes, act, touched = touched_bytes(w, sizes)
+    p1_flops = 4.0 * w.pairs * w.hidden * w.intermediate
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = p1_flops / (p1_ms * 1e-3) / 1e12
+    traffic = profile_traffic(w.name)
+    roof = {"kernel": "grouped_gemm_kernel<1> (phase 1: gate+up GEMM, SiLU·up epilogue)",
+            "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": achieved / tc_peak, "traffic": traffic,
+            "peak_source": f"{src} bf16 dense burst (fp16 dense rate is the same on this part)",
+            "algorithmic_flops_per_launch": p1_flops, "launch_ms": p1_ms}
+    fwd_ms = p1_ms + p2_ms
+    t_flop = flops / (tc_peak * 1e12)
+    t_byte = (wbytes + act) / (hbm * 1e9)
+    forward_roofline = {"t_roof_ms": 1e3 * max(t_flop, t_byte), "t_flop_ms": 1e3 * t_flop,
+                        "t_byte_ms": 1e3 * t_byte, "bound": "tensor" if t_flop >= t_byte else "hbm",
+                        "touched_weight_bytes": wbytes, "activation_bytes": act,
+                        "touched_experts": touched, "phase1_ms": p1_ms, "phase2_ms": p2_ms,
+                        "dispatch_ms": dispatch_ms, "step_ms": ms,
+                        "frac_of_step": 1e3 * max(t_flop, t_byte) / ms,
+                        "peaks": f"{src}: {tc_peak} TFLOP/s, {hbm} GB/s"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = dict(ids_np=d["ids_np"], tw_np=d["tw_np"], x_np=d["x_np"], g=d["gate"].cpu().numpy(),
+                    u=d["up"].cpu().numpy(), d=d["down"].cpu().numpy())
+        rate, desc, threads, secs, _, _ = oracle_sample_rate(w, args.seed, args.cpu_seconds, host=host)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+
+    if rank == 0:
+        clocks = sampler.summary()
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+                "config": config_of(w, "working set larger than L2 (no flush needed)"),
+                "parallelism": "replicas only" if world > 1 else "single GPU",
+                "roofline": roof, "forward_roofline": forward_roofline,
+                "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": 3 * args.steps, "device_status": dev_status,
+                "kernel_source_sha": kernel_source_hash()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

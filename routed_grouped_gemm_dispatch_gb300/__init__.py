@@ -1,0 +1,201 @@
+"""Python binding of the routed fused-MoE expert GEMM library (GB300, sm_103a).
+
+Argument marshalling only: every step runs in the CUDA library
+``_build/libmoe_gb300.so`` through its C ABI (``include/moe_gb300.h``).
+PyTorch provides device memory and the current stream.  There is no CPU or
+PyTorch fallback: if the library is missing or the device is not an sm_103
+part, every call raises.
+
+Calls (names follow "Fused MoE GEMM 提交说明", §提交文件 / §完整算子代码, and
+"moe_dispatch_contract.py"):
+
+  build_dispatch(topk_ids, n_experts)           -> dict of the four int32 tables
+  fused_forward(stacked_expert_tokens, gate_w, up_w, down_w,
+                routed_expert_weights, group_sizes, group_offsets,
+                group_padded_offsets, group_idx_for_bx, up_logits, out)
+  run_kernel(...)                               the page's signature (no up_logits;
+                                                a cached workspace is used)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+BLOCK_TOKEN = 128
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_DEV_BAD_EXPERT_ID = 0x1
+MOE_DEV_BAD_TABLE = 0x2
+MOE_DEV_TIMEOUT = 0x4
+MOE_RUN_PHASE1 = 0x1
+MOE_RUN_PHASE2 = 0x2
+MOE_NO_PDL = 0x4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    """A call of the C ABI returned a MOE_ERR_* status."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built ({LIB_PATH}); call build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.moe_abi_version.argtypes = []
+        L.moe_abi_version.restype = i32
+        L.moe_status_string.argtypes = [i32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_num_blocks.argtypes = [i64, i32, i32]
+        L.moe_num_blocks.restype = i64
+        L.moe_build_dispatch.argtypes = [P, i64, i32, i32, i32, P, P, P, P, i64, P, P]
+        L.moe_build_dispatch.restype = i32
+        L.moe_fused_forward.argtypes = [P, i64, i32, P, P, P, i32, i32, P, i64,
+                                        P, P, P, P, i64, P, P, P, P]
+        L.moe_fused_forward.restype = i32
+        L.moe_fused_forward_ex.argtypes = L.moe_fused_forward.argtypes + [ctypes.c_uint32]
+        L.moe_fused_forward_ex.restype = i32
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def num_blocks(pairs: int, n_experts: int, block_token: int = BLOCK_TOKEN) -> int:
+    return int(lib().moe_num_blocks(int(pairs), int(n_experts), int(block_token)))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t, name, dtype, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def build_dispatch(topk_ids, n_experts: int, block_token: int = BLOCK_TOKEN,
+                   status=None, stream=None, out=None) -> dict:
+    """The four dispatch tables for ``topk_ids`` [T, k] int32 (device).
+
+    ``out`` may supply preallocated tables (same keys as the result)."""
+    import torch
+    ids = _dev(topk_ids, "topk_ids", torch.int32, 2)
+    T, k = ids.shape
+    E = int(n_experts)
+    m = num_blocks(T * k, E, block_token)
+    if out is None:
+        dev = ids.device
+        out = {
+            "group_sizes": torch.empty(E, dtype=torch.int32, device=dev),
+            "group_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "group_padded_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "group_idx_for_bx": torch.empty(max(m, 0), dtype=torch.int32, device=dev),
+        }
+    st = lib().moe_build_dispatch(
+        _ptr(ids), T, k, E, int(block_token), _ptr(out["group_sizes"]), _ptr(out["group_offsets"]),
+        _ptr(out["group_padded_offsets"]), _ptr(out["group_idx_for_bx"]), m,
+        _ptr(status), _stream(stream))
+    _check(st, "moe_build_dispatch")
+    return out
+
+
+def fused_forward(stacked_expert_tokens, gate_w, up_w, down_w, routed_expert_weights,
+                  group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                  up_logits, out, status=None, stream=None,
+                  flags: int = MOE_RUN_PHASE1 | MOE_RUN_PHASE2):
+    """Phase 1 + phase 2 on the current stream; writes ``up_logits`` and ``out``
+    in place on valid rows only.  ``flags`` selects phases (MOE_RUN_PHASE1 /
+    MOE_RUN_PHASE2, optionally MOE_NO_PDL)."""
+    import torch
+    x = _dev(stacked_expert_tokens, "stacked_expert_tokens", torch.float16, 2)
+    g = _dev(gate_w, "gate_w", torch.float16, 3)
+    u = _dev(up_w, "up_w", torch.float16, 3)
+    d = _dev(down_w, "down_w", torch.float16, 3)
+    rw = _dev(routed_expert_weights, "routed_expert_weights", torch.float32, 1)
+    sizes = _dev(group_sizes, "group_sizes", torch.int32, 1)
+    offs = _dev(group_offsets, "group_offsets", torch.int32, 1)
+    padded = _dev(group_padded_offsets, "group_padded_offsets", torch.int32, 1)
+    gidx = _dev(group_idx_for_bx, "group_idx_for_bx", torch.int32, 1)
+    ul = _dev(up_logits, "up_logits", torch.float16, 2)
+    o = _dev(out, "out", torch.float16, 2)
+    rows, H = x.shape
+    E, I, H2 = g.shape
+    if H2 != H or tuple(u.shape) != (E, I, H) or tuple(d.shape) != (E, H, I):
+        raise ValueError("weight shapes do not match [E, I, H] / [E, H, I]")
+    if tuple(ul.shape) != (rows, I) or tuple(o.shape) != (rows, H):
+        raise ValueError("up_logits / out shapes do not match the padded rows")
+    if sizes.numel() != E or offs.numel() < E or padded.numel() < E:
+        raise ValueError("table lengths do not match n_experts")
+    args = (_ptr(x), rows, H, _ptr(g), _ptr(u), _ptr(d), E, I, _ptr(rw), rw.numel(),
+            _ptr(sizes), _ptr(offs), _ptr(padded), _ptr(gidx), gidx.numel(),
+            _ptr(ul), _ptr(o), _ptr(status), _stream(stream))
+    if flags == (MOE_RUN_PHASE1 | MOE_RUN_PHASE2):
+        _check(lib().moe_fused_forward(*args), "moe_fused_forward")
+    else:
+        _check(lib().moe_fused_forward_ex(*args, int(flags)), "moe_fused_forward_ex")
+    return o
+
+
+_WORKSPACE = {}
+
+
+def run_kernel(stacked_expert_tokens, gate_w, up_w, down_w, routed_expert_weights,
+               group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx, out):
+    """The page's submission signature: ``up_logits`` comes from a per-device,
+    per-shape workspace cache (allocated once by PyTorch); ``out`` is written in
+    place; no synchronisation, no new tensor."""
+    import torch
+    key = (stacked_expert_tokens.device.index, int(stacked_expert_tokens.shape[0]),
+           int(gate_w.shape[1]))
+    ws = _WORKSPACE.get(key)
+    if ws is None:
+        ws = torch.empty((key[1], key[2]), dtype=torch.float16, device=stacked_expert_tokens.device)
+        _WORKSPACE[key] = ws
+    fused_forward(stacked_expert_tokens, gate_w, up_w, down_w, routed_expert_weights,
+                  group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx, ws, out)

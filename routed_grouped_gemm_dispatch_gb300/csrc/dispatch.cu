@@ -1,0 +1,127 @@
+// Dispatch-table builder: histogram + exclusive scans + block -> expert map,
+// in one CTA ("moe_dispatch_contract.py", TileLang tutorial ch. 18: module
+// docstring and build_contract; the padded step is ceil((count+1)/padding_M) *
+// padding_M with padding_M = block_token).
+//
+// One CTA of 1024 threads: the counts of up to MOE_MAX_EXPERTS experts live in
+// shared memory, the scans are warp-shuffle scans over one expert per thread,
+// and each block finds its expert by binary search over the padded offsets
+// (the page scans linearly; both give the last expert whose padded start is
+// <= bx * block_token).  No workspace and no host synchronisation: the tables
+// never leave the device.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/moe_gb300.h"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int DISPATCH_THREADS = 1024;
+
+__device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(DISPATCH_THREADS)
+build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32_t n_experts,
+                      int32_t block_token, int32_t* __restrict__ sizes, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ padded, int32_t* __restrict__ gidx, int64_t num_blocks_m,
+                      int32_t* status) {
+    __shared__ int32_t cnt[MOE_MAX_EXPERTS];
+    __shared__ int32_t pad_s[MOE_MAX_EXPERTS + 1];
+    __shared__ int32_t wsum_c[DISPATCH_THREADS / 32];
+    __shared__ int32_t wsum_p[DISPATCH_THREADS / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
+    __syncthreads();
+
+    // histogram of the flattened expert ids
+    bool bad = false;
+    int64_t f = tid;
+    for (; f + 3 * DISPATCH_THREADS < pairs; f += 4 * DISPATCH_THREADS) {
+        int32_t v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldg(topk_ids + f + u * DISPATCH_THREADS);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (static_cast<uint32_t>(v[u]) < static_cast<uint32_t>(n_experts)) atomicAdd(&cnt[v[u]], 1);
+            else bad = true;
+        }
+    }
+    for (; f < pairs; f += DISPATCH_THREADS) {
+        const int32_t v = __ldg(topk_ids + f);
+        if (static_cast<uint32_t>(v) < static_cast<uint32_t>(n_experts)) atomicAdd(&cnt[v], 1);
+        else bad = true;
+    }
+    if (bad && status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+    __syncthreads();
+
+    // exclusive scans of the counts (compact offsets) and of the padded steps
+    const int e = tid;                                  // n_experts <= 1024 threads
+    const int32_t c = e < n_experts ? cnt[e] : 0;
+    const int32_t step = e < n_experts ? ((c + 1 + block_token - 1) / block_token) * block_token : 0;
+    const int32_t ic = warp_incl_scan(c, lane);
+    const int32_t ip = warp_incl_scan(step, lane);
+    if (lane == 31) {
+        wsum_c[warp] = ic;
+        wsum_p[warp] = ip;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t sc = warp_incl_scan(wsum_c[lane], lane);
+        const int32_t sp = warp_incl_scan(wsum_p[lane], lane);
+        wsum_c[lane] = sc;
+        wsum_p[lane] = sp;
+    }
+    __syncthreads();
+    const int32_t base_c = warp > 0 ? wsum_c[warp - 1] : 0;
+    const int32_t base_p = warp > 0 ? wsum_p[warp - 1] : 0;
+    const int32_t excl_c = base_c + ic - c;
+    const int32_t excl_p = base_p + ip - step;
+    if (e < n_experts) {
+        sizes[e] = c;
+        offsets[e] = excl_c;
+        padded[e] = excl_p;
+        pad_s[e] = excl_p;
+    }
+    if (e == n_experts - 1) {
+        offsets[n_experts] = excl_c + c;
+        padded[n_experts] = excl_p + step;
+        pad_s[n_experts] = excl_p + step;
+    }
+    __syncthreads();
+
+    // block -> expert: last e in [0, E) with pad_s[e] <= bx * block_token
+    for (int64_t bx = tid; bx < num_blocks_m; bx += DISPATCH_THREADS) {
+        const int64_t start = bx * block_token;
+        int32_t lo = 0, hi = n_experts - 1;             // pad_s[0] = 0 <= start
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (static_cast<int64_t>(pad_s[mid]) <= start) lo = mid;
+            else hi = mid - 1;
+        }
+        gidx[bx] = lo;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_build_dispatch(const int32_t* topk_ids, int64_t pairs, int32_t n_experts,
+                                  int32_t block_token, int32_t* sizes, int32_t* offsets,
+                                  int32_t* padded, int32_t* gidx, int64_t num_blocks_m,
+                                  int32_t* status, cudaStream_t stream) {
+    build_dispatch_kernel<<<1, DISPATCH_THREADS, 0, stream>>>(topk_ids, pairs, n_experts, block_token, sizes,
+                                                              offsets, padded, gidx, num_blocks_m, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,145 @@
+// C ABI of the library: argument validation and dispatch to the launchers.
+// Every check here runs on the host before anything is enqueued; a failed
+// check returns a MOE_ERR_* code and launches nothing.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/moe_gb300.h"
+#include "moe_internal.h"
+
+namespace {
+
+constexpr int32_t ABI_VERSION = 1;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_device() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_DEVICE;
+    // The library is compiled for sm_103a only.
+    if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+    return MOE_OK;
+}
+
+moe_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    if (e == cudaErrorNotSupported || e == cudaErrorNoDevice) return MOE_ERR_DEVICE;
+    return MOE_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_NULL: return "MOE_ERR_NULL: a required pointer is NULL";
+        case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE: a size is negative, inconsistent or not a multiple of 128";
+        case MOE_ERR_ALIGN: return "MOE_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case MOE_ERR_BLOCK: return "MOE_ERR_BLOCK: block_token must be 128";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: no usable sm_103 device or driver entry point";
+        case MOE_ERR_LAUNCH: return "MOE_ERR_LAUNCH: a kernel launch failed";
+        case MOE_ERR_LIMIT: return "MOE_ERR_LIMIT: n_experts or num_blocks_m above the library limits";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+        default: return "unknown moe status";
+    }
+}
+
+int64_t moe_num_blocks(int64_t pairs, int32_t n_experts, int32_t block_token) {
+    if (pairs < 0 || n_experts < 0 || block_token <= 0) return -1;
+    return (pairs + block_token - 1) / block_token + n_experts;
+}
+
+moe_status_t moe_build_dispatch(const int32_t* topk_ids, int64_t n_tokens, int32_t top_k,
+                                int32_t n_experts, int32_t block_token, int32_t* group_sizes,
+                                int32_t* group_offsets, int32_t* group_padded_offsets,
+                                int32_t* group_idx_for_bx, int64_t num_blocks_m, int32_t* status_dev,
+                                void* stream) {
+    if (n_tokens < 0 || top_k <= 0) return MOE_ERR_SHAPE;
+    if (block_token != MOE_BLOCK_TOKEN) return MOE_ERR_BLOCK;
+    if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return MOE_ERR_LIMIT;
+    const int64_t pairs = n_tokens * static_cast<int64_t>(top_k);
+    if (num_blocks_m != moe_num_blocks(pairs, n_experts, block_token)) return MOE_ERR_SHAPE;
+    if (num_blocks_m > MOE_MAX_BLOCKS) return MOE_ERR_LIMIT;
+    if ((pairs > 0 && !topk_ids) || !group_sizes || !group_offsets || !group_padded_offsets ||
+        !group_idx_for_bx)
+        return MOE_ERR_NULL;
+    if (moe_status_t s = check_device()) return s;
+    return from_cuda(moe::launch_build_dispatch(topk_ids, pairs, n_experts, block_token, group_sizes,
+                                                group_offsets, group_padded_offsets, group_idx_for_bx,
+                                                num_blocks_m, status_dev,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,
+                                  int32_t hidden, const uint16_t* gate_w, const uint16_t* up_w,
+                                  const uint16_t* down_w, int32_t n_experts, int32_t intermediate,
+                                  const float* routed_expert_weights, int64_t total_valid_tokens,
+                                  const int32_t* group_sizes, const int32_t* group_offsets,
+                                  const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx,
+                                  int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out,
+                                  int32_t* status_dev, void* stream, uint32_t flags) {
+    const uint32_t phases = flags & (MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
+    if (phases == 0 || (flags & ~(MOE_RUN_PHASE1 | MOE_RUN_PHASE2 | MOE_NO_PDL)) != 0)
+        return MOE_ERR_SHAPE;
+    if (!stacked_expert_tokens || !gate_w || !up_w || !down_w || !routed_expert_weights ||
+        !group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx || !up_logits ||
+        !out)
+        return MOE_ERR_NULL;
+    if (hidden <= 0 || intermediate <= 0 || hidden % 128 != 0 || intermediate % 128 != 0)
+        return MOE_ERR_SHAPE;
+    if (total_padded_tokens < 0 || total_valid_tokens < 0 || num_blocks_m < 0) return MOE_ERR_SHAPE;
+    if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return MOE_ERR_LIMIT;
+    if (num_blocks_m > MOE_MAX_BLOCKS) return MOE_ERR_LIMIT;
+    if (total_padded_tokens < num_blocks_m * MOE_BLOCK_TOKEN) return MOE_ERR_SHAPE;
+    if (!aligned16(stacked_expert_tokens) || !aligned16(gate_w) || !aligned16(up_w) ||
+        !aligned16(down_w) || !aligned16(up_logits) || !aligned16(out))
+        return MOE_ERR_ALIGN;
+    if (moe_status_t s = check_device()) return s;
+    if (num_blocks_m == 0) return MOE_OK;
+
+    moe::ForwardArgs a{};
+    a.x = stacked_expert_tokens;
+    a.rows_total = total_padded_tokens;
+    a.hidden = hidden;
+    a.gate_w = gate_w;
+    a.up_w = up_w;
+    a.down_w = down_w;
+    a.n_experts = n_experts;
+    a.intermediate = intermediate;
+    a.rw = routed_expert_weights;
+    a.valid_total = total_valid_tokens;
+    a.sizes = group_sizes;
+    a.offsets = group_offsets;
+    a.padded = group_padded_offsets;
+    a.gidx = group_idx_for_bx;
+    a.num_blocks_m = num_blocks_m;
+    a.up_logits = up_logits;
+    a.out = out;
+    a.status = status_dev;
+    return from_cuda(moe::launch_fused_forward(a, flags, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_fused_forward(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,
+                               int32_t hidden, const uint16_t* gate_w, const uint16_t* up_w,
+                               const uint16_t* down_w, int32_t n_experts, int32_t intermediate,
+                               const float* routed_expert_weights, int64_t total_valid_tokens,
+                               const int32_t* group_sizes, const int32_t* group_offsets,
+                               const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx,
+                               int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out,
+                               int32_t* status_dev, void* stream) {
+    return moe_fused_forward_ex(stacked_expert_tokens, total_padded_tokens, hidden, gate_w, up_w, down_w,
+                                n_experts, intermediate, routed_expert_weights, total_valid_tokens,
+                                group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                                num_blocks_m, up_logits, out, status_dev, stream,
+                                MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
+}
+
+}  // extern "C"

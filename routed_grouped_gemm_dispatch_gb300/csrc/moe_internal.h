@@ -1,0 +1,43 @@
+// Declarations shared by the translation units of the library (host side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+struct ForwardArgs {
+    const uint16_t* x;            // [rows_total, H]
+    int64_t rows_total;
+    int32_t hidden;
+    const uint16_t* gate_w;       // [E, I, H]
+    const uint16_t* up_w;         // [E, I, H]
+    const uint16_t* down_w;       // [E, H, I]
+    int32_t n_experts;
+    int32_t intermediate;
+    const float* rw;              // [valid_total]
+    int64_t valid_total;
+    const int32_t* sizes;
+    const int32_t* offsets;
+    const int32_t* padded;
+    const int32_t* gidx;
+    int64_t num_blocks_m;
+    uint16_t* up_logits;          // [rows_total, I]
+    uint16_t* out;                // [rows_total, H]
+    int32_t* status;
+};
+
+// Enqueue the dispatch-table builder.  Arguments already validated.
+cudaError_t launch_build_dispatch(const int32_t* topk_ids, int64_t pairs, int32_t n_experts,
+                                  int32_t block_token, int32_t* sizes, int32_t* offsets,
+                                  int32_t* padded, int32_t* gidx, int64_t num_blocks_m,
+                                  int32_t* status, cudaStream_t stream);
+
+// Enqueue phase 1 and/or phase 2 (MOE_RUN_* flags).  Arguments already validated.  Returns
+// cudaErrorNotSupported when the driver entry point for tensor maps is missing.
+cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream);
+
+// Multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace moe
