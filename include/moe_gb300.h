@@ -107,6 +107,7 @@ moe_status_t moe_build_dispatch(const int32_t* topk_ids, int64_t n_tokens, int32
  *   gate_w, up_w          [n_experts, intermediate, hidden] fp16
  *   down_w                [n_experts, hidden, intermediate] fp16
  *   routed_expert_weights [total_valid_tokens] fp32, compact (expert-sorted) order
+ *                         (may be NULL when total_valid_tokens == 0)
  *   group_*               the four tables above (only entries [0, n_experts) of
  *                         group_offsets / group_padded_offsets are read)
  *   up_logits             [total_padded_tokens, intermediate] fp16 workspace

@@ -89,8 +89,8 @@ moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t
     const uint32_t phases = flags & (MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
     if (phases == 0 || (flags & ~(MOE_RUN_PHASE1 | MOE_RUN_PHASE2 | MOE_NO_PDL)) != 0)
         return MOE_ERR_SHAPE;
-    if (!stacked_expert_tokens || !gate_w || !up_w || !down_w || !routed_expert_weights ||
-        !group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx || !up_logits ||
+    if (!stacked_expert_tokens || !gate_w || !up_w || !down_w ||
+        (total_valid_tokens > 0 && !routed_expert_weights) || !group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx || !up_logits ||
         !out)
         return MOE_ERR_NULL;
     if (hidden <= 0 || intermediate <= 0 || hidden % 128 != 0 || intermediate % 128 != 0)
