@@ -53,6 +53,7 @@ typedef int32_t moe_status_t;
 #define MOE_ERR_LAUNCH   -6  /* a kernel launch failed (cudaGetLastError)            */
 #define MOE_ERR_LIMIT    -7  /* n_experts or num_blocks_m above the library limits   */
 #define MOE_ERR_WORKSPACE -8 /* workspace missing or smaller than required           */
+#define MOE_ERR_STATIC_WORKSPACE -9 /* problem larger than the library's fixed workspace */
 
 /* Bits OR-ed into *status_dev by kernels. */
 #define MOE_DEV_BAD_EXPERT_ID 0x1  /* a topk id outside [0, n_experts)                 */
@@ -149,6 +150,40 @@ moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t
                                   const int32_t* group_idx_for_bx, int64_t num_blocks_m,
                                   uint16_t* up_logits, uint16_t* out,
                                   int32_t* status_dev, void* stream, uint32_t flags);
+
+/* Size of the fixed workspace used by moe_fused_forward_static_workspace. */
+#define MOE_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+
+/* The fused forward for callers that cannot allocate device memory (the pages
+ * have no counterpart of this call).  A plugin inside an inference runtime
+ * that owns every device allocation, or a latency-critical serving loop that
+ * cannot afford cudaMalloc's possible device-wide synchronisation or its
+ * failure under memory pressure, cannot provide the up_logits workspace that
+ * moe_fused_forward needs.  This call takes the same arguments without
+ * up_logits and keeps that workspace in a fixed array compiled into the
+ * library: every GPU that loads the library holds MOE_STATIC_WORKSPACE_BYTES
+ * (64 MiB) of device memory for it until the process exits.
+ *   - Limit: total_padded_tokens * intermediate * 2 bytes must not exceed
+ *     MOE_STATIC_WORKSPACE_BYTES; larger problems return
+ *     MOE_ERR_STATIC_WORKSPACE and nothing is enqueued.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls in the process share the one array per device and it keeps
+ *     the last call's contents.  Nothing in it has to start at zero.  Calls
+ *     whose kernels overlap on the GPU (different streams, no ordering between
+ *     them) race on the array and give wrong results; order them.
+ * Otherwise the same arguments, requirements, results and errors as
+ * moe_fused_forward. */
+moe_status_t moe_fused_forward_static_workspace(
+    const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens, int32_t hidden,
+    const uint16_t* gate_w, const uint16_t* up_w, const uint16_t* down_w,
+    int32_t n_experts, int32_t intermediate,
+    const float* routed_expert_weights, int64_t total_valid_tokens,
+    const int32_t* group_sizes, const int32_t* group_offsets,
+    const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx, int64_t num_blocks_m,
+    uint16_t* out, int32_t* status_dev, void* stream);
 
 #ifdef __cplusplus
 }

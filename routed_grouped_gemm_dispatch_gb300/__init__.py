@@ -76,6 +76,9 @@ def lib():
         L.moe_fused_forward.restype = i32
         L.moe_fused_forward_ex.argtypes = L.moe_fused_forward.argtypes + [ctypes.c_uint32]
         L.moe_fused_forward_ex.restype = i32
+        L.moe_fused_forward_static_workspace.argtypes = [P, i64, i32, P, P, P, i32, i32, P, i64,
+                                                         P, P, P, P, i64, P, P, P]
+        L.moe_fused_forward_static_workspace.restype = i32
         _lib = L
         return L
 
@@ -179,6 +182,35 @@ def fused_forward(stacked_expert_tokens, gate_w, up_w, down_w, routed_expert_wei
         _check(lib().moe_fused_forward(*args), "moe_fused_forward")
     else:
         _check(lib().moe_fused_forward_ex(*args, int(flags)), "moe_fused_forward_ex")
+    return o
+
+
+def fused_forward_static_workspace(stacked_expert_tokens, gate_w, up_w, down_w,
+                                   routed_expert_weights, group_sizes, group_offsets,
+                                   group_padded_offsets, group_idx_for_bx, out,
+                                   status=None, stream=None):
+    """The fused forward without an up_logits argument, for callers that
+    cannot allocate device memory: the workspace is the library's fixed
+    64 MiB array (total_padded_tokens * intermediate * 2 bytes at most).
+    Calls share that array, so calls that overlap on the GPU race."""
+    import torch
+    x = _dev(stacked_expert_tokens, "stacked_expert_tokens", torch.float16, 2)
+    g = _dev(gate_w, "gate_w", torch.float16, 3)
+    u = _dev(up_w, "up_w", torch.float16, 3)
+    d = _dev(down_w, "down_w", torch.float16, 3)
+    rw = _dev(routed_expert_weights, "routed_expert_weights", torch.float32, 1)
+    tabs = [_dev(t, n, torch.int32, 1) for t, n in
+            ((group_sizes, "group_sizes"), (group_offsets, "group_offsets"),
+             (group_padded_offsets, "group_padded_offsets"), (group_idx_for_bx, "group_idx_for_bx"))]
+    o = _dev(out, "out", torch.float16, 2)
+    rows, H = x.shape
+    E, I, _ = g.shape
+    if tuple(o.shape) != (rows, H):
+        raise ValueError("out shape does not match the padded rows")
+    st = lib().moe_fused_forward_static_workspace(
+        _ptr(x), rows, H, _ptr(g), _ptr(u), _ptr(d), E, I, _ptr(rw), rw.numel(),
+        *[_ptr(t) for t in tabs], tabs[3].numel(), _ptr(o), _ptr(status), _stream(stream))
+    _check(st, "moe_fused_forward_static_workspace")
     return o
 
 

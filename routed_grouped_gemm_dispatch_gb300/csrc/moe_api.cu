@@ -48,6 +48,9 @@ const char* moe_status_string(moe_status_t s) {
         case MOE_ERR_LAUNCH: return "MOE_ERR_LAUNCH: a kernel launch failed";
         case MOE_ERR_LIMIT: return "MOE_ERR_LIMIT: n_experts or num_blocks_m above the library limits";
         case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+        case MOE_ERR_STATIC_WORKSPACE:
+            return "MOE_ERR_STATIC_WORKSPACE: total_padded_tokens * intermediate * 2 bytes exceeds the "
+                   "library's fixed workspace (MOE_STATIC_WORKSPACE_BYTES)";
         default: return "unknown moe status";
     }
 }

@@ -1,0 +1,80 @@
+"""moe_fused_forward_static_workspace: the forward for callers that cannot
+allocate device memory (a plugin inside a runtime that owns all device
+allocations, or a latency-critical loop that cannot risk cudaMalloc's
+synchronisation or failure), checked through the C ABI against
+moe_fused_forward on the same inputs, two calls in a row.
+
+The file is named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import routed_grouped_gemm_dispatch_gb300 as moe
+import workloads
+from gpu_side import bits, gpu_prepare, run_forward, sentinel
+from moe_cases import raw_inputs, small_workload, within_tol
+
+MOE_ERR_STATIC_WORKSPACE = -9
+STATIC_BYTES = 64 * 1024 * 1024
+
+
+def _call_static(side, out, status):
+    t = side.tables
+    x = side.x_packed
+    rows, H = x.shape
+    E, I, _ = side.gate.shape
+    return moe.lib().moe_fused_forward_static_workspace(
+        x.data_ptr(), rows, H, side.gate.data_ptr(), side.up.data_ptr(), side.down.data_ptr(),
+        E, I, side.rw.data_ptr() if side.rw.numel() else None, side.rw.numel(),
+        t["group_sizes"].data_ptr(), t["group_offsets"].data_ptr(),
+        t["group_padded_offsets"].data_ptr(), t["group_idx_for_bx"].data_ptr(),
+        t["group_idx_for_bx"].numel(), out.data_ptr(), status.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+
+
+def _valid_rows(side):
+    return np.sort(side.pair_rows.cpu().numpy().reshape(-1))
+
+
+@pytest.mark.gpu
+def test_static_workspace_matches_regular_entry_two_calls_in_a_row():
+    cases = [workloads.WORKLOADS["decode_skewed"],
+             small_workload(tokens=300, top_k=2, experts=3, hidden=256, intermediate=384)]
+    sides = []
+    for w in cases:
+        side = gpu_prepare(raw_inputs(w, seed=5))
+        assert side.rows_total * w.intermediate * 2 <= STATIC_BYTES
+        _, ref = run_forward(side, w.intermediate)
+        sides.append((w, side, bits(ref)))
+    # two calls in a row on each case, and a different case in between, so a
+    # call never sees a workspace left in its own state by the call before
+    for w, side, ref in sides + sides[:1]:
+        for _ in range(2):
+            out = sentinel(side.rows_total, w.hidden)
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            rc = _call_static(side, out, status)
+            assert rc == 0, moe.status_string(rc)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            got = bits(out)
+            v = _valid_rows(side)
+            pad = np.ones(side.rows_total, bool)
+            pad[v] = False
+            assert np.array_equal(got[pad], ref[pad])          # padding rows untouched
+            ok = within_tol(got[v], ref[v], 2e-2, 2e-2)
+            assert ok.all(), f"{np.count_nonzero(~ok)} outputs outside tolerance"
+
+
+def test_static_workspace_rejects_problems_above_its_limit():
+    moe.build()
+    L = moe.lib()
+    rows, inter = 128 * 300, 1024           # 300 blocks x 1024 x 2 B = 75 MiB > 64 MiB
+    assert rows * inter * 2 > STATIC_BYTES
+    fake = ctypes.c_void_p(0x1000)
+    rc = L.moe_fused_forward_static_workspace(fake, rows, 256, fake, fake, fake, 4, inter, fake, 10,
+                                              fake, fake, fake, fake, 300, fake, None, None)
+    assert rc == MOE_ERR_STATIC_WORKSPACE
+    assert "fixed workspace" in moe.status_string(rc)
