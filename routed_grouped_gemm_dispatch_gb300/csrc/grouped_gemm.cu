@@ -11,20 +11,36 @@
 // with e = group_idx_for_bx[bx], token_offset = bx·128 − group_padded_offsets[e],
 // actual_rows = max(0, min(128, group_sizes[e] − token_offset)).
 //
-// GB300 design (not the page's): one persistent CTA per SM walks a compacted
-// list of active (block, slice) tiles, so padding-only blocks cost nothing.
-// Warp roles: warp 0 issues TMA loads (128-byte swizzled tiles, 4-stage
-// ring), warp 1 owns TMEM and issues tcgen05.mma (M=128, N=256, K=16, fp32
-// accumulators in TMEM, double buffered so the epilogue of tile t overlaps the
-// MMAs of tile t+1), warps 2-5 run the epilogue from TMEM through registers.
-// Phase 1 stacks the gate and up slices as one N=256 B operand so the x tile
-// is loaded once for both products.  Every pipeline wait is bounded.
+// GB300 design (not the page's):
+//  * Persistent clusters of two CTAs (one CTA per SM) walk a compacted list of
+//    work units built from the active blocks (actual_rows > 0), so padding-only
+//    blocks cost nothing.  A unit is a PAIR — two consecutive active blocks of
+//    the same expert — or a SINGLE block.
+//  * Each (unit, N slice) tile is one 2-SM MMA tile: tcgen05.mma.cta_group::2
+//    with M = 256 (rows 0..127 = the first block, held by the even CTA; rows
+//    128..255 = the second block, held by the odd CTA) and N = 256, where each
+//    CTA's shared memory holds only half of the weight tile (128 of its 256
+//    rows) and the pair shares it.  Per SM this halves the weight bytes that
+//    TMA writes into and the tensor core reads out of shared memory, which is
+//    what limits a one-SM 128 x 256 tile.  A single block runs the same tile
+//    with its rows repeated in the odd CTA, whose results are not stored.
+//  * Inside a CTA: warp 0 issues TMA loads (128-byte swizzled tiles, 6-stage
+//    ring; both CTAs' copies complete on the even CTA's "full" barrier), warp 1
+//    owns TMEM (allocated for the pair) and, in the even CTA only, issues the
+//    MMAs (K = 16 each, fp32 accumulators in TMEM, double buffered so the
+//    epilogue of one tile overlaps the MMAs of the next), warps 2-5 run the
+//    epilogue of the CTA's own 128 rows from TMEM through registers.  Phase 1
+//    stacks the gate slice (even CTA) and the up slice (odd CTA) as the N=256 B
+//    operand, so the x tile is read once for both products.  Every pipeline
+//    wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/moe_gb300.h"
 #include "moe_internal.h"
@@ -36,31 +52,35 @@ namespace {
 constexpr int BM = 128;                       // rows per block (block_token)
 constexpr int BK = 64;                        // K per stage: one 128-byte swizzle row
 constexpr int BN = 256;                       // N per MMA
-constexpr int STAGES = 4;
-constexpr int A_TILE_BYTES = BM * BK * 2;     // 16 KB
-constexpr int B_TILE_BYTES = BN * BK * 2;     // 32 KB
-constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 x 256
+constexpr int STAGES = 6;
+constexpr int A_TILE_BYTES = BM * BK * 2;     // 16 KB: this CTA's 128 rows of A
+constexpr int B_HALF_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 rows of B
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_HALF_BYTES;
+constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 lanes x 256
 constexpr int NUM_THREADS = 192;              // 6 warps
 constexpr int NUM_EPI_THREADS = 128;          // warps 2..5
-constexpr int PANEL = 16;                     // active blocks per rasterisation panel
+constexpr int CLUSTER = 2;
+constexpr uint16_t CLUSTER_MASK = 0x3;
+constexpr uint16_t PAIR_BIT = 0x8000;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s per drain wait
-constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
+constexpr uint32_t IDESC = idesc_f16_f32acc(2 * BM, BN);   // M = 256 across the pair
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
+static_assert(MOE_MAX_BLOCKS <= 0x7FFF, "block indices must leave the pair bit free");
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).  During the
+// prologue the stage area also holds the active-block list and its experts.
 constexpr int OFF_STAGES = 0;
 constexpr int OFF_BARS = STAGES * STAGE_BYTES;                 // 8-byte mbarriers
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;               // full, empty, tfull, tempty, drain
 constexpr int OFF_TMEM_SLOT = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
-constexpr int OFF_NACT = OFF_ABORT + 4;
-constexpr int OFF_WSUM = OFF_NACT + 4;                         // NUM_THREADS/32 ints
-constexpr int OFF_LIST = ((OFF_WSUM + (NUM_THREADS / 32) * 4 + 15) / 16) * 16;  // uint16 bx list
+constexpr int OFF_COUNTS = OFF_ABORT + 4;                      // nact, nunits
+constexpr int OFF_WSUM = OFF_COUNTS + 8;                       // NUM_THREADS/32 ints
+constexpr int OFF_UNITS = ((OFF_WSUM + (NUM_THREADS / 32) * 4 + 15) / 16) * 16;
 
-size_t smem_bytes_for(int64_t num_blocks_m) {
-    return 1024 /* alignment slack */ + OFF_LIST + 2 * static_cast<size_t>(num_blocks_m);
-}
+__host__ __device__ inline size_t units_bytes(int64_t m) { return ((2 * static_cast<size_t>(m) + 15) / 16) * 16; }
+size_t smem_bytes_for(int64_t m) { return 1024 /* alignment slack */ + OFF_UNITS + units_bytes(m); }
 
 struct GemmParams {
     const int32_t* sizes;
@@ -79,25 +99,8 @@ struct GemmParams {
     int32_t n_extent;         // I (phase 1) or H (phase 2): columns of dst
 };
 
-struct TileInfo {
-    int32_t bx;
-    int32_t n;
-};
-
-__device__ __forceinline__ TileInfo decode_tile(int32_t t, int32_t nact, int32_t n_tiles,
-                                                const uint16_t* list) {
-    const int32_t per_panel = PANEL * n_tiles;
-    const int32_t pi = t / per_panel;
-    const int32_t r = t - pi * per_panel;
-    const int32_t first = pi * PANEL;
-    const int32_t width = min(PANEL, nact - first);
-    const int32_t n = r / width;
-    const int32_t b = r - n * width;
-    return TileInfo{static_cast<int32_t>(list[first + b]), n};
-}
-
 // Rows of block bx that belong to its expert ("Fused MoE GEMM 提交说明",
-// §完整算子代码: actual_rows).  Also returns the expert and the row's
+// §完整算子代码: actual_rows).  Also returns the expert and the block's
 // token_offset.  Blocks whose table entries point outside their arrays count
 // as empty and raise MOE_DEV_BAD_TABLE.
 __device__ __forceinline__ int32_t block_rows(const GemmParams& p, int32_t bx, int32_t* e_out,
@@ -123,11 +126,34 @@ __device__ __forceinline__ int32_t block_rows(const GemmParams& p, int32_t bx, i
     return static_cast<int32_t>(actual);
 }
 
+// One cluster tile as seen by the CTA of rank `rank`: unit t / n_tiles, slice
+// t % n_tiles.
+struct Tile {
+    int32_t bx0;      // first block of the unit (the expert comes from it)
+    int32_t bx;       // block whose rows this CTA holds
+    int32_t n;        // N slice
+    bool store;       // false: the odd CTA of a single block (repeated rows)
+};
+
+__device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, int32_t n_tiles,
+                                            uint32_t rank) {
+    const int32_t u = t / n_tiles;
+    Tile ti;
+    ti.n = t - u * n_tiles;
+    ti.bx0 = units[u] & 0x7FFF;
+    const bool pair = (units[u] & PAIR_BIT) != 0;
+    ti.bx = pair ? ti.bx0 + static_cast<int32_t>(rank) : ti.bx0;
+    ti.store = pair || rank == 0;
+    return ti;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// map_a: activations (x or up_logits), box 64 x 128 rows; map_b0 / map_b1:
+// phase 1 gate / up (box 64 x 128), phase 2 down (box 64 x 128, map_b1 unused).
 template <int PHASE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -138,30 +164,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + OFF_BARS;                   // [STAGES]
+    const uint32_t bar_full = sbase + OFF_BARS;                   // [STAGES] (used in the even CTA)
     const uint32_t bar_empty = bar_full + 8 * STAGES;             // [STAGES]
     const uint32_t bar_tfull = bar_empty + 8 * STAGES;            // [2]
-    const uint32_t bar_tempty = bar_tfull + 16;                   // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;                   // [2] (used in the even CTA)
     const uint32_t bar_drain = bar_tempty + 16;                   // [1]
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+    int32_t* counts = reinterpret_cast<int32_t*>(smem + OFF_COUNTS);
     int32_t* wsum = reinterpret_cast<int32_t*>(smem + OFF_WSUM);
-    uint16_t* list = reinterpret_cast<uint16_t*>(smem + OFF_LIST);
+    uint16_t* units = reinterpret_cast<uint16_t*>(smem + OFF_UNITS);
+    // prologue scratch in the (still unused) stage area
+    uint16_t* act_bx = reinterpret_cast<uint16_t*>(smem + OFF_STAGES);
+    uint16_t* act_e = act_bx + p.num_blocks_m;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const uint32_t rank = cluster_cta_rank();
+    const bool leader = rank == 0;
 
     if (PHASE == 1) pdl_launch_dependents();
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, 1);           // the even CTA's arrive.expect_tx
+            mbar_init(bar_empty + 8 * s, 1);          // the MMA's commit, multicast to both CTAs
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
-            mbar_init(bar_tempty + 8 * a, NUM_EPI_THREADS);
+            mbar_init(bar_tempty + 8 * a, CLUSTER * NUM_EPI_THREADS);
         }
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -173,19 +205,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         if (PHASE == 1) tma_prefetch_map(&map_b1);
     }
     if (warp == 1) {
-        tmem_alloc(sbase + OFF_TMEM_SLOT, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(sbase + OFF_TMEM_SLOT, TMEM_COLS);
+        tmem_relinquish_pair();
     }
 
-    // ---- compacted list of active blocks (same order as bx) ----------------
+    // ---- 1. compacted list of active blocks and their experts (bx order) ---
     int32_t nact = 0;
     for (int32_t base = 0; base < p.num_blocks_m; base += NUM_THREADS) {
         const int32_t bx = base + tid;
-        int32_t flag = 0;
-        if (bx < p.num_blocks_m) {
-            int32_t e, tok;
-            flag = block_rows(p, bx, &e, &tok) > 0;
-        }
+        int32_t flag = 0, e = 0, tok = 0;
+        if (bx < p.num_blocks_m) flag = block_rows(p, bx, &e, &tok) > 0;
         const uint32_t ballot = __ballot_sync(0xffffffffu, flag);
         if (lane == 0) wsum[warp] = __popc(ballot);
         __syncthreads();
@@ -196,46 +225,87 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             before += (w < warp) ? c : 0;
             total += c;
         }
-        if (flag) list[nact + before + __popc(ballot & ((1u << lane) - 1u))] = static_cast<uint16_t>(bx);
+        if (flag) {
+            const int32_t i = nact + before + __popc(ballot & ((1u << lane) - 1u));
+            act_bx[i] = static_cast<uint16_t>(bx);
+            act_e[i] = static_cast<uint16_t>(e);
+        }
         nact += total;
         __syncthreads();
+    }
+
+    // ---- 2. units: pair up consecutive blocks of one expert ----------------
+    // A run is a maximal stretch of consecutive list entries with the same
+    // expert and consecutive block indices; inside a run, entries at even
+    // positions start a unit, which is a pair when the run continues.
+    if (warp == 0) {
+        int32_t nu = 0, run_start = 0;
+        for (int32_t base = 0; base < nact; base += 32) {
+            const int32_t i = base + lane;
+            const bool in = i < nact;
+            const int32_t bxi = in ? act_bx[i] : 0;
+            const int32_t ei = in ? act_e[i] : -1;
+            const bool cont = in && i > 0 && act_e[i - 1] == ei && act_bx[i - 1] + 1 == bxi;
+            const uint32_t starts = __ballot_sync(0xffffffffu, in && !cont);
+            const uint32_t le = starts & (lane == 31 ? 0xffffffffu : ((2u << lane) - 1u));
+            const int32_t rs = le ? base + 31 - __clz(le) : run_start;
+            const bool ustart = in && (((i - rs) & 1) == 0);
+            const bool next_cont = (i + 1 < nact) && act_e[i + 1] == ei && act_bx[i + 1] == bxi + 1;
+            const uint32_t ub = __ballot_sync(0xffffffffu, ustart);
+            if (ustart)
+                units[nu + __popc(ub & ((1u << lane) - 1u))] =
+                    static_cast<uint16_t>(bxi | (next_cont ? PAIR_BIT : 0));
+            nu += __popc(ub);
+            if (starts) run_start = base + 31 - __clz(starts);
+        }
+        if (lane == 0) {
+            counts[0] = nact;
+            counts[1] = nu;
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int32_t total_tiles = nact * p.n_tiles;
+    const int32_t total_tiles = counts[1] * p.n_tiles;
+    // Both CTAs' barriers are initialised and their prologue scratch in the
+    // stage area is dead before either CTA's copies or commits reach the other.
+    cluster_sync_all();
 
     // Phase 2 reads up_logits written by phase 1: wait for that grid here
     // (everything above only touched the dispatch tables).
     if (PHASE == 2) pdl_wait_prior_grid();
 
+    const int32_t cluster_id = static_cast<int32_t>(blockIdx.x) / CLUSTER;
+    const int32_t n_clusters = static_cast<int32_t>(gridDim.x) / CLUSTER;
+
     if (warp == 0) {
-        // ===================== TMA producer =====================
+        // ===================== TMA producer (both CTAs) =====================
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_normal();
+            const uint32_t leader_full = mapa_shared(bar_full, 0);
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, nact, p.n_tiles, list);
-                const int32_t e = __ldg(p.gidx + ti.bx);
+            for (int32_t t = cluster_id; t < total_tiles && ok; t += n_clusters) {
+                const Tile ti = decode_tile(t, units, p.n_tiles, rank);
+                const int32_t e = __ldg(p.gidx + ti.bx0);
                 for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = bar_full + 8 * stage;
+                    const uint32_t fb = leader_full + 8 * stage;
                     const uint32_t sa = sbase + OFF_STAGES + stage * STAGE_BYTES;
                     const uint32_t sb = sa + A_TILE_BYTES;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    tma_load_2d(sa, &map_a, fb, kb * BK, ti.bx * BM, pol);
-                    if (PHASE == 1) {
-                        tma_load_3d(sb, &map_b0, fb, kb * BK, ti.n * 128, e, pol);
-                        tma_load_3d(sb + B_TILE_BYTES / 2, &map_b1, fb, kb * BK, ti.n * 128, e, pol);
-                    } else {
-                        tma_load_3d(sb, &map_b0, fb, kb * BK, ti.n * BN, e, pol);
-                    }
+                    const int32_t k0 = kb * BK;
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, CLUSTER * STAGE_BYTES);
+                    tma_load_2d_pair(sa, &map_a, fb, k0, ti.bx * BM, pol);
+                    if (PHASE == 1)
+                        tma_load_3d_pair(sb, leader ? &map_b0 : &map_b1, fb, k0, ti.n * 128, e, pol);
+                    else
+                        tma_load_3d_pair(sb, &map_b0, fb, k0, ti.n * BN + static_cast<int32_t>(rank) * 128, e,
+                                         pol);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -243,21 +313,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             if (!ok) {
                 // Let the copies already in flight land before the CTA exits.
                 volatile int never = 0;
-                const int64_t n = issued < STAGES ? issued : STAGES;
-                for (int64_t i = 0; i < n; ++i) {
-                    const int64_t idx = issued - 1 - i;
-                    mbar_wait_bounded(bar_full + 8 * static_cast<uint32_t>(idx % STAGES),
-                                      static_cast<uint32_t>((idx / STAGES) & 1), &never, DRAIN_LIMIT_NS);
+                if (leader) {
+                    const int64_t n = issued < STAGES ? issued : STAGES;
+                    for (int64_t i = 0; i < n; ++i) {
+                        const int64_t idx = issued - 1 - i;
+                        mbar_wait_bounded(bar_full + 8 * static_cast<uint32_t>(idx % STAGES),
+                                          static_cast<uint32_t>((idx / STAGES) & 1), &never, DRAIN_LIMIT_NS);
+                    }
+                } else {
+                    // the odd CTA's copies report to the even CTA's barriers:
+                    // give them a bounded moment to land
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 1000000ull) { }
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ===================== MMA issuer =====================
-        if (lane == 0) {
+        // ===================== MMA issuer (even CTA only) =====================
+        if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
             bool ok = true;
-            for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            for (int32_t t = cluster_id; t < total_tiles && ok; t += n_clusters) {
                 if (!mbar_wait_bounded(bar_tempty + 8 * acc, aphase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                     ok = false;
                     break;
@@ -274,32 +351,34 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_f16(d_tmem, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32),
-                                   IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16_pair(d_tmem, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32),
+                                        IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    tc_commit(bar_empty + 8 * stage);
+                    // the slot may be refilled in both CTAs once these MMAs are done
+                    tc_commit_pair_mc(bar_empty + 8 * stage, CLUSTER_MASK);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit(bar_tfull + 8 * acc);
+                tc_commit_pair_mc(bar_tfull + 8 * acc, CLUSTER_MASK);
                 acc ^= 1u;
                 if (acc == 0) aphase ^= 1u;
             }
             // Every MMA this thread issued has finished once this arrives.
             volatile int never = 0;
-            tc_commit(bar_drain);
+            tc_commit_pair(bar_drain);
             mbar_wait_bounded(bar_drain, 0, &never, DRAIN_LIMIT_NS);
         }
         __syncwarp();
     } else {
-        // ===================== epilogue (warps 2..5) =====================
+        // ===================== epilogue (warps 2..5, both CTAs) =====================
         const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
-        const int row = quarter * 32 + lane;         // row of the 128-row tile
+        const int row = quarter * 32 + lane;         // row of this CTA's 128-row block
+        const uint32_t leader_tempty = mapa_shared(bar_tempty, 0);
         uint32_t acc = 0, aphase = 0;
-        for (int32_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile(t, nact, p.n_tiles, list);
+        for (int32_t t = cluster_id; t < total_tiles; t += n_clusters) {
+            const Tile ti = decode_tile(t, units, p.n_tiles, rank);
             int32_t e = 0, tok = 0;
-            const int32_t actual = block_rows(p, ti.bx, &e, &tok);
+            const int32_t actual = ti.store ? block_rows(p, ti.bx, &e, &tok) : 0;
             if (!mbar_wait_bounded(bar_tfull + 8 * acc, aphase, abort_flag, WAIT_LIMIT_NS)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
@@ -353,7 +432,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
             }
             tc_fence_before_sync();
-            mbar_arrive(bar_tempty + 8 * acc);
+            // the accumulator may be reused once both CTAs have read their rows
+            if (leader) mbar_arrive(bar_tempty + 8 * acc);
+            else mbar_arrive_cluster(leader_tempty + 8 * acc);
             acc ^= 1u;
             if (acc == 0) aphase ^= 1u;
         }
@@ -361,10 +442,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
     tc_fence_before_sync();
     __syncthreads();
+    // Neither CTA leaves (or frees the pair's TMEM) while the other may still
+    // write into its shared memory, arrive on its barriers or use the TMEM.
+    cluster_sync_all();
     if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -416,8 +500,33 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t experts, uint64_t ro
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t set_smem_attr(const void* fn, size_t bytes) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+// Clusters of two that can be resident at once for a kernel with `smem`
+// bytes of dynamic shared memory (cached per device, kernel and size).
+template <int PHASE>
+int max_clusters(size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, size_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(dev, smem);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(CLUSTER * 64);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<PHASE>, &cfg) != cudaSuccess) n = 0;
+    cache[key] = n;
+    return n;
 }
 
 }  // namespace
@@ -437,7 +546,7 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     const uint64_t E = static_cast<uint64_t>(a.n_experts);
     if (!make_map_2d(&map_x, a.x, rows, H, BM) || !make_map_3d(&map_gate, a.gate_w, E, I, H, 128) ||
         !make_map_3d(&map_up, a.up_w, E, I, H, 128) || !make_map_2d(&map_u, a.up_logits, rows, I, BM) ||
-        !make_map_3d(&map_down, a.down_w, E, H, I, BN))
+        !make_map_3d(&map_down, a.down_w, E, H, I, 128))
         return cudaErrorInvalidValue;
 
     GemmParams p1{};
@@ -462,31 +571,42 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     p2.n_extent = a.hidden;
 
     const size_t smem = smem_bytes_for(a.num_blocks_m);
-    cudaError_t err;
-    if ((err = set_smem_attr(reinterpret_cast<const void*>(&grouped_gemm_kernel<1>), smem)) != cudaSuccess) return err;
-    if ((err = set_smem_attr(reinterpret_cast<const void*>(&grouped_gemm_kernel<2>), smem)) != cudaSuccess) return err;
+    cudaError_t err = cudaSuccess;
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem))) != cudaSuccess)
+        return err;
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem))) != cudaSuccess)
+        return err;
 
-    const int sms = device_sm_count();
-    if (sms <= 0) return cudaErrorNoDevice;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
 
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(sms));
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cfg.numAttrs = 0;
+    cfg.attrs = attr;
     if (flags & MOE_RUN_PHASE1) {
+        const int nc = max_clusters<1>(smem);
+        if (nc <= 0) return cudaErrorNoDevice;
+        cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
+        cfg.numAttrs = 1;
         err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_gate, map_up, p1);
         if (err != cudaSuccess) return err;
     }
     if (flags & MOE_RUN_PHASE2) {
         // Phase 2 may start its prologue (tables, TMEM, barriers) while phase 1
         // drains; it waits for phase 1's results before its first load.
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = (flags & MOE_NO_PDL) ? 0 : 1;
+        const int nc = max_clusters<2>(smem);
+        if (nc <= 0) return cudaErrorNoDevice;
+        cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
+        cfg.numAttrs = (flags & MOE_NO_PDL) ? 1 : 2;
         err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_down, map_down, p2);
     }
     return err;
