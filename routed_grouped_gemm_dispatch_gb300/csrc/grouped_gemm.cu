@@ -50,11 +50,14 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;                       // rows per block (block_token)
-constexpr int BK = 64;                        // K per stage: one 128-byte swizzle row
+constexpr int BK = 64;                        // K per box: one 128-byte swizzle row
+constexpr int KSUB = 1;                       // boxes (adjacent 64-wide K chunks) per stage
 constexpr int BN = 256;                       // N per MMA
-constexpr int STAGES = 6;
-constexpr int A_TILE_BYTES = BM * BK * 2;     // 16 KB: this CTA's 128 rows of A
-constexpr int B_HALF_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 rows of B
+constexpr int STAGES = 6 / KSUB;
+constexpr int A_BOX_BYTES = BM * BK * 2;      // 16 KB: this CTA's 128 rows of A, one box
+constexpr int B_BOX_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 rows of B, one box
+constexpr int A_TILE_BYTES = KSUB * A_BOX_BYTES;
+constexpr int B_HALF_BYTES = KSUB * B_BOX_BYTES;
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_HALF_BYTES;
 constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 lanes x 256
 constexpr int NUM_THREADS = 192;              // 6 warps
@@ -62,6 +65,7 @@ constexpr int NUM_EPI_THREADS = 128;          // warps 2..5
 constexpr int CLUSTER = 2;
 constexpr uint16_t CLUSTER_MASK = 0x3;
 constexpr uint16_t PAIR_BIT = 0x8000;
+constexpr int SMALL_ROWS = 32;                // blocks with at most this many rows load 16-row boxes
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s per drain wait
 constexpr uint32_t IDESC = idesc_f16_f32acc(2 * BM, BN);   // M = 256 across the pair
@@ -132,7 +136,8 @@ struct Tile {
     int32_t bx0;      // first block of the unit (the expert comes from it)
     int32_t bx;       // block whose rows this CTA holds
     int32_t n;        // N slice
-    bool store;       // false: the odd CTA of a single block (repeated rows)
+    bool pair;
+    bool store;       // false: the odd CTA of a single block (its rows are discarded)
 };
 
 __device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, int32_t n_tiles,
@@ -141,9 +146,9 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, in
     Tile ti;
     ti.n = t - u * n_tiles;
     ti.bx0 = units[u] & 0x7FFF;
-    const bool pair = (units[u] & PAIR_BIT) != 0;
-    ti.bx = pair ? ti.bx0 + static_cast<int32_t>(rank) : ti.bx0;
-    ti.store = pair || rank == 0;
+    ti.pair = (units[u] & PAIR_BIT) != 0;
+    ti.bx = ti.pair ? ti.bx0 + static_cast<int32_t>(rank) : ti.bx0;
+    ti.store = ti.pair || rank == 0;
     return ti;
 }
 
@@ -152,11 +157,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// map_a: activations (x or up_logits), box 64 x 128 rows; map_b0 / map_b1:
-// phase 1 gate / up (box 64 x 128), phase 2 down (box 64 x 128, map_b1 unused).
+// map_a / map_a16: activations (x or up_logits), boxes of 64 x 128 and 64 x 16
+// rows; map_b0 / map_b1: phase 1 gate / up (box 64 x 128), phase 2 down (box
+// 64 x 128, map_b1 unused).
 template <int PHASE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_a16,
                     const __grid_constant__ CUtensorMap map_b0,
                     const __grid_constant__ CUtensorMap map_b1,
                     const GemmParams p) {
@@ -201,6 +208,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_a16);
         tma_prefetch_map(&map_b0);
         if (PHASE == 1) tma_prefetch_map(&map_b1);
     }
@@ -239,7 +247,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // expert and consecutive block indices; inside a run, entries at even
     // positions start a unit, which is a pair when the run continues.
     if (warp == 0) {
-        int32_t nu = 0, run_start = 0;
+        int32_t nu = 0, run_start = 0, nruns = 0;
         for (int32_t base = 0; base < nact; base += 32) {
             const int32_t i = base + lane;
             const bool in = i < nact;
@@ -256,10 +264,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 units[nu + __popc(ub & ((1u << lane) - 1u))] =
                     static_cast<uint16_t>(bxi | (next_cont ? PAIR_BIT : 0));
             nu += __popc(ub);
+            nruns += __popc(starts);
             if (starts) run_start = base + 31 - __clz(starts);
         }
         if (lane == 0) {
-            counts[0] = nact;
+            counts[0] = nruns;
             counts[1] = nu;
         }
     }
@@ -268,6 +277,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const int32_t total_tiles = counts[1] * p.n_tiles;
+    // With about one unit per expert run every weight byte is used once:
+    // stream the weights through L2 with evict-first; otherwise keep them for
+    // the expert's other units.
+    const bool weights_streamed = 4 * counts[1] <= 5 * counts[0];
     // Both CTAs' barriers are initialised and their prologue scratch in the
     // stage area is dead before either CTA's copies or commits reach the other.
     cluster_sync_all();
@@ -282,14 +295,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if (warp == 0) {
         // ===================== TMA producer (both CTAs) =====================
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_normal();
+            const uint64_t pol_a = l2_policy_evict_normal();   // activations
+            const uint64_t pol_b = weights_streamed ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint32_t leader_full = mapa_shared(bar_full, 0);
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
+            // Tile metadata is fetched ahead of use so that no global-memory
+            // round trip sits between two tiles' copies: the expert of tile
+            // t + 2C and that expert's size and padded offset for tile t + C
+            // are loaded while tile t streams (C = number of clusters).
+            auto expert_of = [&](int32_t tt) -> int32_t {
+                return tt < total_tiles ? __ldg(p.gidx + decode_tile(tt, units, p.n_tiles, rank).bx0) : 0;
+            };
+            int32_t e_cur = expert_of(cluster_id);
+            int32_t size_cur = __ldg(p.sizes + e_cur), pad_cur = __ldg(p.padded + e_cur);
+            int32_t e_next = expert_of(cluster_id + n_clusters);
             for (int32_t t = cluster_id; t < total_tiles && ok; t += n_clusters) {
                 const Tile ti = decode_tile(t, units, p.n_tiles, rank);
-                const int32_t e = __ldg(p.gidx + ti.bx0);
+                const int32_t e = e_cur;
+                const int32_t size_next = __ldg(p.sizes + e_next), pad_next = __ldg(p.padded + e_next);
+                const int32_t e_next2 = expert_of(t + 2 * n_clusters);
+                // Rows of A to load: none for the odd CTA of a single block
+                // (its rows of D are discarded, stale shared memory serves);
+                // 16-row boxes for a block with at most SMALL_ROWS valid rows
+                // (decode-like blocks); otherwise the full 128-row box, which
+                // moves faster than many small boxes.  Rows not loaded only
+                // feed discarded rows of D.  (Only the even CTA, which sets the
+                // expected byte count, needs the odd CTA's count.)
+                auto a_boxes = [&](int32_t bx) -> int32_t {   // 0: full box
+                    int32_t r = size_cur - (bx * BM - pad_cur);
+                    r = r > BM ? BM : (r < 0 ? 0 : r);
+                    return r > SMALL_ROWS ? 0 : (r + 15) / 16;
+                };
+                auto a_bytes = [&](int32_t boxes) -> uint32_t {
+                    return boxes == 0 ? A_BOX_BYTES : boxes * (A_BOX_BYTES / 8);
+                };
+                const bool load_a = ti.store;
+                const int32_t boxes_own = load_a ? a_boxes(ti.bx) : 0;
+                const uint32_t bytes_peer = (leader && ti.pair) ? a_bytes(a_boxes(ti.bx0 + 1)) : 0;
+                const uint32_t stage_tx =
+                    KSUB * ((load_a ? a_bytes(boxes_own) : 0) + bytes_peer + 2 * B_BOX_BYTES);
                 for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -298,17 +344,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const uint32_t fb = leader_full + 8 * stage;
                     const uint32_t sa = sbase + OFF_STAGES + stage * STAGE_BYTES;
                     const uint32_t sb = sa + A_TILE_BYTES;
-                    const int32_t k0 = kb * BK;
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, CLUSTER * STAGE_BYTES);
-                    tma_load_2d_pair(sa, &map_a, fb, k0, ti.bx * BM, pol);
-                    if (PHASE == 1)
-                        tma_load_3d_pair(sb, leader ? &map_b0 : &map_b1, fb, k0, ti.n * 128, e, pol);
-                    else
-                        tma_load_3d_pair(sb, &map_b0, fb, k0, ti.n * BN + static_cast<int32_t>(rank) * 128, e,
-                                         pol);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, stage_tx);
+#pragma unroll
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        const int32_t k0 = (kb * KSUB + ks) * BK;
+                        if (load_a && boxes_own == 0) {
+                            tma_load_2d_pair(sa + ks * A_BOX_BYTES, &map_a, fb, k0, ti.bx * BM, pol_a);
+                        } else if (load_a) {
+                            for (int32_t b = 0; b < boxes_own; ++b)
+                                tma_load_2d_pair(sa + ks * A_BOX_BYTES + b * (A_BOX_BYTES / 8), &map_a16, fb, k0,
+                                                 ti.bx * BM + b * 16, pol_a);
+                        }
+                        if (PHASE == 1)
+                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, leader ? &map_b0 : &map_b1, fb, k0, ti.n * 128,
+                                             e, pol_b);
+                        else
+                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, &map_b0, fb, k0,
+                                             ti.n * BN + static_cast<int32_t>(rank) * 128, e, pol_b);
+                    }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                e_cur = e_next;
+                size_cur = size_next;
+                pad_cur = pad_next;
+                e_next = e_next2;
             }
             if (!ok) {
                 // Let the copies already in flight land before the CTA exits.
@@ -350,8 +410,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const uint32_t sa = sbase + OFF_STAGES + stage * STAGE_BYTES;
                     const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_f16_pair(d_tmem, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32),
+                    for (int kk = 0; kk < KSUB * (BK / 16); ++kk) {
+                        const uint32_t off = (kk / (BK / 16)) * A_BOX_BYTES + (kk % (BK / 16)) * 32;
+                        const uint32_t offb = (kk / (BK / 16)) * B_BOX_BYTES + (kk % (BK / 16)) * 32;
+                        tc_mma_f16_pair(d_tmem, smem_desc_k_sw128(sa + off), smem_desc_k_sw128(sb + offb),
                                         IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
                     // the slot may be refilled in both CTAs once these MMAs are done
@@ -540,12 +602,13 @@ int device_sm_count() {
 
 cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream) {
     if (!encode_fn()) return cudaErrorNotSupported;
-    CUtensorMap map_x, map_gate, map_up, map_u, map_down;
+    CUtensorMap map_x, map_x16, map_gate, map_up, map_u, map_u16, map_down;
     const uint64_t rows = static_cast<uint64_t>(a.rows_total);
     const uint64_t H = static_cast<uint64_t>(a.hidden), I = static_cast<uint64_t>(a.intermediate);
     const uint64_t E = static_cast<uint64_t>(a.n_experts);
-    if (!make_map_2d(&map_x, a.x, rows, H, BM) || !make_map_3d(&map_gate, a.gate_w, E, I, H, 128) ||
-        !make_map_3d(&map_up, a.up_w, E, I, H, 128) || !make_map_2d(&map_u, a.up_logits, rows, I, BM) ||
+    if (!make_map_2d(&map_x, a.x, rows, H, BM) || !make_map_2d(&map_x16, a.x, rows, H, 16) ||
+        !make_map_3d(&map_gate, a.gate_w, E, I, H, 128) || !make_map_3d(&map_up, a.up_w, E, I, H, 128) ||
+        !make_map_2d(&map_u, a.up_logits, rows, I, BM) || !make_map_2d(&map_u16, a.up_logits, rows, I, 16) ||
         !make_map_3d(&map_down, a.down_w, E, H, I, 128))
         return cudaErrorInvalidValue;
 
@@ -562,11 +625,11 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     p1.n_experts = a.n_experts;
     GemmParams p2 = p1;
     p1.dst = a.up_logits;
-    p1.k_blocks = a.hidden / BK;
+    p1.k_blocks = a.hidden / (BK * KSUB);
     p1.n_tiles = a.intermediate / 128;
     p1.n_extent = a.intermediate;
     p2.dst = a.out;
-    p2.k_blocks = a.intermediate / BK;
+    p2.k_blocks = a.intermediate / (BK * KSUB);
     p2.n_tiles = (a.hidden + BN - 1) / BN;
     p2.n_extent = a.hidden;
 
@@ -597,7 +660,7 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_gate, map_up, p1);
+        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x16, map_gate, map_up, p1);
         if (err != cudaSuccess) return err;
     }
     if (flags & MOE_RUN_PHASE2) {
@@ -607,7 +670,7 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = (flags & MOE_NO_PDL) ? 1 : 2;
-        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_down, map_down, p2);
+        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_u16, map_down, map_down, p2);
     }
     return err;
 }
