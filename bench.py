@@ -184,22 +184,17 @@ def prepare_device(w, seed, dev):
     T, k = ids_np.shape
     ids = torch.from_numpy(ids_np).to(dev)
     tables = moe.build_dispatch(ids, w.experts)
-    flat = ids.reshape(-1).long()
-    P = flat.numel()
-    order = torch.sort(flat, stable=True).indices
-    e_sorted = flat[order]
-    rank = torch.arange(P, device=dev) - tables["group_offsets"].long()[e_sorted]
-    rows = torch.empty(P, dtype=torch.long, device=dev)
-    rows[order] = tables["group_padded_offsets"].long()[e_sorted] + rank
     rows_total = tables["group_idx_for_bx"].numel() * moe.BLOCK_TOKEN
-    xp = torch.full((rows_total, w.hidden), float("nan"), dtype=torch.float16, device=dev)
-    xp[rows] = torch.from_numpy(x_np).to(dev)[torch.arange(P, device=dev) // k]
-    rw = torch.from_numpy(tw_np).to(dev).reshape(-1)[order].contiguous()
+    x_tok = torch.from_numpy(x_np).to(dev)
+    tw = torch.from_numpy(tw_np).to(dev)
+    pk = moe.pack_routed(ids, tw, x_tok, tables, rows_total)
+    xp, rw, rows = pk["stacked_expert_tokens"], pk["routed_expert_weights"], pk["pair_padded_rows"]
     ul = torch.zeros((rows_total, w.intermediate), dtype=torch.float16, device=dev)
     out = torch.zeros((rows_total, w.hidden), dtype=torch.float16, device=dev)
     torch.cuda.synchronize(dev)
     return dict(ids=ids, tables=tables, xp=xp, rw=rw, ul=ul, out=out, gate=gate, up=up, down=down,
-                ids_np=ids_np, tw_np=tw_np, x_np=x_np, rows_total=rows_total, pair_rows=rows)
+                ids_np=ids_np, tw_np=tw_np, x_np=x_np, rows_total=rows_total, pair_rows=rows,
+                x_tok=x_tok, tw=tw)
 
 
 def touched_bytes(w, sizes):
@@ -395,20 +390,34 @@ def main():
     dev_status = int(status.item())
 
     # ---- end to end through the public API with host buffers ---------------
+    # token-major inputs in pinned host memory -> H2D -> dispatch tables ->
+    # pack -> phase 1 + phase 2 -> combine -> D2H of the token outputs
     e2e = None
     if not args.no_e2e:
         h_ids = d["ids"].cpu().pin_memory()
-        h_x = d["xp"].cpu().pin_memory()
-        h_rw = d["rw"].cpu().pin_memory()
-        h_out = torch.empty_like(d["out"], device="cpu").pin_memory()
+        h_x = d["x_tok"].cpu().pin_memory()
+        h_tw = d["tw"].cpu().pin_memory()
+        T = h_x.shape[0]
+        h_y = torch.empty((T, w.hidden), dtype=torch.float16).pin_memory()
+        d_ids, d_x, d_tw = torch.empty_like(d["ids"]), torch.empty_like(d["x_tok"]), torch.empty_like(d["tw"])
+        d_y = torch.empty((T, w.hidden), dtype=torch.float16, device=dev)
+        ws = torch.empty(max(16, int(moe.lib().moe_pack_workspace_bytes(w.pairs, E))), dtype=torch.uint8,
+                         device=dev)
+        prows = torch.empty((T, w.top_k), dtype=torch.int32, device=dev)
         n_e2e = max(5, min(args.steps, 100))
 
         def e2e_step():
-            d["ids"].copy_(h_ids, non_blocking=True)
-            d["xp"].copy_(h_x, non_blocking=True)
-            d["rw"].copy_(h_rw, non_blocking=True)
-            step()
-            h_out.copy_(d["out"], non_blocking=True)
+            d_ids.copy_(h_ids, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+            d_tw.copy_(h_tw, non_blocking=True)
+            moe.build_dispatch(d_ids, E, out=t)
+            moe.pack_routed(d_ids, d_tw, d_x, t, d["rows_total"], stacked=d["xp"], routed_weights=d["rw"],
+                            pair_rows=prows, workspace=ws)
+            moe.fused_forward(d["xp"], d["gate"], d["up"], d["down"], d["rw"], t["group_sizes"],
+                              t["group_offsets"], t["group_padded_offsets"], t["group_idx_for_bx"],
+                              d["ul"], d["out"])
+            moe.combine_routed(d["out"], prows, y=d_y)
+            h_y.copy_(d_y, non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -420,13 +429,13 @@ def main():
         b.record()
         torch.cuda.synchronize(dev)
         e2e_ms = a.elapsed_time(b) / n_e2e
-        h2d = h_ids.numel() * 4 + h_x.numel() * 2 + h_rw.numel() * 4
-        d2h = h_out.numel() * 2
+        h2d = h_ids.numel() * 4 + h_x.numel() * 2 + h_tw.numel() * 4
+        d2h = h_y.numel() * 2
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": n_e2e,
-               "path": "pinned host topk_ids + stacked tokens + routed weights -> H2D -> "
-                       "moe_build_dispatch -> moe_fused_forward -> D2H out"}
+               "steps": n_e2e, "gpu_launches_per_step": 8,
+               "path": "pinned host tokens [T,H] + topk_ids + topk weights -> H2D -> moe_build_dispatch -> "
+                       "moe_pack_routed -> moe_fused_forward -> moe_combine_routed -> D2H token outputs [T,H]"}
 
     # ---- roofline --------------------------------------------------------------
     peaks, src = load_peaks()

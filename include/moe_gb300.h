@@ -129,6 +129,50 @@ moe_status_t moe_fused_forward(const uint16_t* stacked_expert_tokens, int64_t to
                                uint16_t* up_logits, uint16_t* out,
                                int32_t* status_dev, void* stream);
 
+/* Workspace bytes moe_pack_routed needs for `pairs` (token, expert) pairs
+ * (per-chunk expert histograms and every pair's rank inside its chunk).
+ * Returns -1 for invalid arguments. */
+int64_t moe_pack_workspace_bytes(int64_t pairs, int32_t n_experts);
+
+/* Pack: place every (token, expert) pair in the grouped, padded layout that
+ * moe_fused_forward reads.  Pairs are stably sorted by expert
+ * ("moe_dispatch_contract.py", build_contract), so the pair of rank r inside
+ * expert e (counting pairs in flat order t*top_k + j) goes to padded row
+ * group_padded_offsets[e] + r and compact index group_offsets[e] + r
+ * ("Fused MoE GEMM 提交说明", §实现要点).
+ *   topk_ids, topk_weights  [n_tokens, top_k] int32 / fp32 (weights may be NULL
+ *                           when routed_expert_weights is NULL)
+ *   x_tokens                [n_tokens, hidden] fp16 (may be NULL when
+ *                           stacked_expert_tokens is NULL)
+ *   group_offsets, group_padded_offsets  the tables of moe_build_dispatch
+ *   stacked_expert_tokens   out, nullable: [total_padded_tokens, hidden]; row
+ *                           pair_padded_rows[f] receives x_tokens[f / top_k];
+ *                           padding rows are not written
+ *   routed_expert_weights   out, nullable: [n_tokens*top_k] fp32, compact order
+ *   pair_padded_rows        out: [n_tokens, top_k] int32 padded row of every
+ *                           pair (-1 for an id outside [0, n_experts))
+ *   workspace               device scratch of moe_pack_workspace_bytes() bytes
+ * Three kernel launches; an out-of-range id sets MOE_DEV_BAD_EXPERT_ID. */
+moe_status_t moe_pack_routed(const int32_t* topk_ids, const float* topk_weights, int64_t n_tokens,
+                             int32_t top_k, int32_t n_experts, const uint16_t* x_tokens, int32_t hidden,
+                             const int32_t* group_offsets, const int32_t* group_padded_offsets,
+                             int64_t total_padded_tokens, uint16_t* stacked_expert_tokens,
+                             float* routed_expert_weights, int32_t* pair_padded_rows,
+                             void* workspace, size_t workspace_bytes, int32_t* status_dev, void* stream);
+
+/* Combine: y[t, :] = fp16( sum over j = 0..top_k-1, in that order, of
+ * out[pair_padded_rows[t*top_k + j], :] ) with the sum in fp32 and one
+ * round-to-nearest-even.  The pages combine with a PyTorch scatter_reduce
+ * ("MetaX-TileLang工具链", §2.7); the routed weight is already inside `out`.
+ *   out               [total_padded_tokens, hidden] fp16 (moe_fused_forward's)
+ *   pair_padded_rows  [n_tokens, top_k] int32 (moe_pack_routed's); negative
+ *                     entries are skipped
+ *   y                 out: [n_tokens, hidden] fp16
+ * One kernel launch. */
+moe_status_t moe_combine_routed(const uint16_t* out, int64_t total_padded_tokens, int32_t hidden,
+                                const int32_t* pair_padded_rows, int64_t n_tokens, int32_t top_k,
+                                uint16_t* y, void* stream);
+
 /* Flags of moe_fused_forward_ex. */
 #define MOE_RUN_PHASE1   0x1u  /* gate+up GEMM and SiLU·up epilogue into up_logits   */
 #define MOE_RUN_PHASE2   0x2u  /* down GEMM and routed-weight epilogue into out       */

@@ -15,6 +15,8 @@ Calls (names follow "Fused MoE GEMM æäº¤è¯´æ˜Ž", Â§æäº¤æ–‡ä»¶ / Â§å®Œæ•´ç®—å
                 group_padded_offsets, group_idx_for_bx, up_logits, out)
   run_kernel(...)                               the page's signature (no up_logits;
                                                 a cached workspace is used)
+  pack_routed(topk_ids, topk_weights, x_tokens, tables)  -> grouped, padded inputs
+  combine_routed(out, pair_rows)                -> token-major sum of the expert rows
 """
 from __future__ import annotations
 
@@ -79,6 +81,13 @@ def lib():
         L.moe_fused_forward_static_workspace.argtypes = [P, i64, i32, P, P, P, i32, i32, P, i64,
                                                          P, P, P, P, i64, P, P, P]
         L.moe_fused_forward_static_workspace.restype = i32
+        L.moe_pack_workspace_bytes.argtypes = [i64, i32]
+        L.moe_pack_workspace_bytes.restype = i64
+        L.moe_pack_routed.argtypes = [P, P, i64, i32, i32, P, i32, P, P, i64, P, P, P, P,
+                                      ctypes.c_size_t, P, P]
+        L.moe_pack_routed.restype = i32
+        L.moe_combine_routed.argtypes = [P, i64, i32, P, i64, i32, P, P]
+        L.moe_combine_routed.restype = i32
         _lib = L
         return L
 
@@ -212,6 +221,55 @@ def fused_forward_static_workspace(stacked_expert_tokens, gate_w, up_w, down_w,
         *[_ptr(t) for t in tabs], tabs[3].numel(), _ptr(o), _ptr(status), _stream(stream))
     _check(st, "moe_fused_forward_static_workspace")
     return o
+
+
+def pack_routed(topk_ids, topk_weights, x_tokens, tables, rows_total: int | None = None,
+                stacked=None, routed_weights=None, pair_rows=None, workspace=None,
+                status=None, stream=None) -> dict:
+    """Grouped, padded activations, compact routed weights and every pair's
+    padded row, from token-major inputs (all device tensors).  Preallocated
+    outputs may be passed; padding rows of ``stacked`` are left untouched
+    (a new ``stacked`` is filled with fp16 NaN there)."""
+    import torch
+    ids = _dev(topk_ids, "topk_ids", torch.int32, 2)
+    T, k = ids.shape
+    E = tables["group_sizes"].numel()
+    x = _dev(x_tokens, "x_tokens", torch.float16, 2) if x_tokens is not None else None
+    tw = _dev(topk_weights, "topk_weights", torch.float32, 2) if topk_weights is not None else None
+    H = x.shape[1] if x is not None else 128
+    if rows_total is None:
+        rows_total = tables["group_idx_for_bx"].numel() * BLOCK_TOKEN
+    dev = ids.device
+    if stacked is None and x is not None:
+        stacked = torch.full((rows_total, H), float("nan"), dtype=torch.float16, device=dev)
+    if routed_weights is None and tw is not None:
+        routed_weights = torch.empty(T * k, dtype=torch.float32, device=dev)
+    if pair_rows is None:
+        pair_rows = torch.empty((T, k), dtype=torch.int32, device=dev)
+    need = int(lib().moe_pack_workspace_bytes(T * k, E))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib().moe_pack_routed(
+        _ptr(ids), _ptr(tw), T, k, E, _ptr(x), H, _ptr(tables["group_offsets"]),
+        _ptr(tables["group_padded_offsets"]), rows_total, _ptr(stacked), _ptr(routed_weights),
+        _ptr(pair_rows), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check(st, "moe_pack_routed")
+    return {"stacked_expert_tokens": stacked, "routed_expert_weights": routed_weights,
+            "pair_padded_rows": pair_rows}
+
+
+def combine_routed(out, pair_rows, y=None, stream=None):
+    """y[t] = fp16(sum_j out[pair_rows[t, j]]) with an fp32 sum in j order."""
+    import torch
+    o = _dev(out, "out", torch.float16, 2)
+    pr = _dev(pair_rows, "pair_rows", torch.int32, 2)
+    T, k = pr.shape
+    if y is None:
+        y = torch.empty((T, o.shape[1]), dtype=torch.float16, device=o.device)
+    st = lib().moe_combine_routed(_ptr(o), o.shape[0], o.shape[1], _ptr(pr), T, k, _ptr(y),
+                                  _stream(stream))
+    _check(st, "moe_combine_routed")
+    return y
 
 
 _WORKSPACE = {}

@@ -81,6 +81,49 @@ moe_status_t moe_build_dispatch(const int32_t* topk_ids, int64_t n_tokens, int32
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+int64_t moe_pack_workspace_bytes(int64_t pairs, int32_t n_experts) {
+    if (pairs < 0 || n_experts <= 0) return -1;
+    return moe::pack_workspace_bytes(pairs, n_experts);
+}
+
+moe_status_t moe_pack_routed(const int32_t* topk_ids, const float* topk_weights, int64_t n_tokens, int32_t top_k,
+                             int32_t n_experts, const uint16_t* x_tokens, int32_t hidden,
+                             const int32_t* group_offsets, const int32_t* group_padded_offsets,
+                             int64_t total_padded_tokens, uint16_t* stacked_expert_tokens,
+                             float* routed_expert_weights, int32_t* pair_padded_rows, void* workspace,
+                             size_t workspace_bytes, int32_t* status_dev, void* stream) {
+    if (n_tokens < 0 || top_k <= 0 || hidden <= 0 || hidden % 128 != 0 || total_padded_tokens < 0)
+        return MOE_ERR_SHAPE;
+    if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return MOE_ERR_LIMIT;
+    const int64_t pairs = n_tokens * static_cast<int64_t>(top_k);
+    if (pairs == 0) return MOE_OK;
+    if (!topk_ids || !group_offsets || !group_padded_offsets || !pair_padded_rows) return MOE_ERR_NULL;
+    if (stacked_expert_tokens && !x_tokens) return MOE_ERR_NULL;
+    if (routed_expert_weights && !topk_weights) return MOE_ERR_NULL;
+    if ((stacked_expert_tokens && (!aligned16(stacked_expert_tokens) || !aligned16(x_tokens))))
+        return MOE_ERR_ALIGN;
+    if (!workspace || static_cast<int64_t>(workspace_bytes) < moe::pack_workspace_bytes(pairs, n_experts))
+        return MOE_ERR_WORKSPACE;
+    if (moe_status_t s = check_device()) return s;
+    return from_cuda(moe::launch_pack(topk_ids, topk_weights, n_tokens, top_k, n_experts, x_tokens, hidden,
+                                      group_offsets, group_padded_offsets, total_padded_tokens, pairs,
+                                      stacked_expert_tokens, routed_expert_weights, pair_padded_rows, workspace,
+                                      status_dev, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine_routed(const uint16_t* out, int64_t total_padded_tokens, int32_t hidden,
+                                const int32_t* pair_padded_rows, int64_t n_tokens, int32_t top_k, uint16_t* y,
+                                void* stream) {
+    if (n_tokens < 0 || top_k <= 0 || hidden <= 0 || hidden % 128 != 0 || total_padded_tokens < 0)
+        return MOE_ERR_SHAPE;
+    if (n_tokens == 0) return MOE_OK;
+    if (!out || !pair_padded_rows || !y) return MOE_ERR_NULL;
+    if (!aligned16(out) || !aligned16(y)) return MOE_ERR_ALIGN;
+    if (moe_status_t s = check_device()) return s;
+    return from_cuda(moe::launch_combine(out, total_padded_tokens, hidden, pair_padded_rows, n_tokens, top_k, y,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,
                                   int32_t hidden, const uint16_t* gate_w, const uint16_t* up_w,
                                   const uint16_t* down_w, int32_t n_experts, int32_t intermediate,

@@ -37,6 +37,17 @@ cudaError_t launch_build_dispatch(const int32_t* topk_ids, int64_t pairs, int32_
 // cudaErrorNotSupported when the driver entry point for tensor maps is missing.
 cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream);
 
+// Pack: pair ranks, padded rows, compact routed weights, activation rows.
+int64_t pack_workspace_bytes(int64_t pairs, int32_t n_experts);
+cudaError_t launch_pack(const int32_t* topk_ids, const float* topk_weights, int64_t n_tokens, int32_t top_k,
+                        int32_t n_experts, const uint16_t* x_tokens, int32_t hidden, const int32_t* offsets,
+                        const int32_t* padded, int64_t rows_total, int64_t valid_total, uint16_t* x_packed,
+                        float* rw_compact, int32_t* pair_rows, void* workspace, int32_t* status,
+                        cudaStream_t stream);
+// Combine: y[t] = fp16(sum_j out[pair_rows[t*k + j]]) in fp32, j in order.
+cudaError_t launch_combine(const uint16_t* out, int64_t rows_total, int32_t hidden, const int32_t* pair_rows,
+                           int64_t n_tokens, int32_t top_k, uint16_t* y, cudaStream_t stream);
+
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 

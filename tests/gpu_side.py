@@ -2,9 +2,8 @@
 library, and the grouped/padded packing of tokens.
 
 Shares nothing with the oracle side: the tables come from
-``moe_build_dispatch``; the packing is plain PyTorch indexing on the device
-(a stable sort by expert, each pair's rank within its expert), written from the
-contract's description, not from the oracle.
+``moe_build_dispatch`` and the packing from ``moe_pack_routed``, both CUDA
+kernels of the library.
 """
 from __future__ import annotations
 
@@ -21,7 +20,7 @@ from moe_cases import BT, SENTINEL, Raw
 class GpuSide:
     ids: torch.Tensor
     tables: dict
-    pair_rows: torch.Tensor       # int64 [T, k]
+    pair_rows: torch.Tensor       # int32 [T, k]
     rows_total: int
     x_packed: torch.Tensor        # fp16 [rows_total, H]
     rw: torch.Tensor              # fp32 [P]
@@ -36,26 +35,17 @@ def to_device_weights(raw: Raw, device="cuda"):
 
 
 def gpu_prepare(raw: Raw, weights=None, device="cuda") -> GpuSide:
-    T, k = raw.topk_ids.shape
-    E, H = raw.w.experts, raw.w.hidden
+    """Tables from moe_build_dispatch, packing from moe_pack_routed."""
+    E = raw.w.experts
     ids = torch.from_numpy(np.ascontiguousarray(raw.topk_ids)).to(device)
     t = moe.build_dispatch(ids, E)
-    flat = ids.reshape(-1).long()
-    P = flat.numel()
-    order = torch.sort(flat, stable=True).indices
-    e_sorted = flat[order]
-    rank = torch.arange(P, device=device) - t["group_offsets"].long()[e_sorted]
-    rows = torch.empty(P, dtype=torch.long, device=device)
-    rows[order] = t["group_padded_offsets"].long()[e_sorted] + rank
+    x = torch.from_numpy(np.ascontiguousarray(raw.x_tokens)).to(device)
+    tw = torch.from_numpy(np.ascontiguousarray(raw.topk_weights)).to(device)
     rows_total = t["group_idx_for_bx"].numel() * BT
-    x = torch.from_numpy(raw.x_tokens).to(device)
-    xp = torch.full((rows_total, H), float("nan"), dtype=torch.float16, device=device)
-    if P:
-        xp[rows] = x[torch.arange(P, device=device) // k]
-    tw = torch.from_numpy(raw.topk_weights).to(device).reshape(-1)
-    rw = tw[order].contiguous()                 # compact index of sorted position i is i
+    pk = moe.pack_routed(ids, tw, x, t, rows_total)
     g, u, d = weights if weights is not None else to_device_weights(raw, device)
-    return GpuSide(ids, t, rows.reshape(T, k), rows_total, xp, rw, g, u, d)
+    return GpuSide(ids, t, pk["pair_padded_rows"], rows_total, pk["stacked_expert_tokens"],
+                   pk["routed_expert_weights"], g, u, d)
 
 
 def sentinel(rows: int, cols: int, device="cuda") -> torch.Tensor:
