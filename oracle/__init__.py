@@ -11,7 +11,8 @@ module only builds that library and marshals numpy arrays into it.
 Pages followed (title, section):
   * "Fused MoE GEMM 提交说明" — §算子来源, §实现要点, §完整算子代码
   * "moe_dispatch_contract.py" (TileLang tutorial ch. 18) — docstring, build_contract
-  * "MetaX-TileLang工具链" — §1.9, §1.12.1, §2.4
+  * "MetaX-TileLang工具链" — §1.9, §1.12.1, §2.4 (also the router: logits,
+    softmax, top-k)
 """
 from __future__ import annotations
 
@@ -78,6 +79,8 @@ def _load():
         lib.oracle_pack.restype = ctypes.c_int
         lib.oracle_combine.argtypes = [P, i64, i32, P, i64, i32, P]
         lib.oracle_combine.restype = ctypes.c_int
+        lib.oracle_router.argtypes = [P, i64, i32, P, i32, i32, P, P, i32]
+        lib.oracle_router.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -263,3 +266,20 @@ def combine(out, pair_rows, n_tokens: int, top_k: int):
     if rc != 0:
         raise ValueError("oracle_combine rejected its input")
     return y
+
+
+def router(x_tokens, router_w, top_k: int, n_threads: int = 0):
+    """topk_ids int32 [T, k] and topk_weights fp32 [T, k] ("MetaX-TileLang工具链"
+    §2.4: logits -> softmax -> top-k)."""
+    x = _bits16(x_tokens)
+    w = _bits16(router_w)
+    T, H = x.shape
+    E, H2 = w.shape
+    if H2 != H:
+        raise ValueError("router weight shape mismatch")
+    ids = np.zeros((T, top_k), np.int32)
+    wts = np.zeros((T, top_k), np.float32)
+    rc = _load().oracle_router(_ptr(x), T, H, _ptr(w), E, int(top_k), _ptr(ids), _ptr(wts), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_router rejected its input")
+    return ids, wts

@@ -19,7 +19,7 @@
  *        padded offsets, m_blocks, block -> expert map), and its three checks.
  *   [P3] "MetaX-TileLang工具链" — §1.9 (the two launches and their arguments),
  *        §1.12.1 and §2.4 (gate = SiLU(x W_gate), up = x W_up, mid = gate*up,
- *        out = mid W_down).
+ *        out = mid W_down; the router: logits = W_g(x), softmax, top-k).
  *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - fp32 -> fp16 conversion is IEEE-754 round-to-nearest-even, overflow to inf.
@@ -33,7 +33,9 @@
  * Parity pins: every function here is pinned by a -m "not gpu" test (fp16
  * conversion against numpy over all bit patterns, tables against [P2]'s
  * invariants and hand-derived examples, the forward against closed forms and a
- * tables-free brute force).  No function is "parity unpinned".
+ * tables-free brute force, the router against one-hot weights whose logits
+ * are the token's own values and a float64 brute force).  No function is
+ * "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -427,6 +429,58 @@ int oracle_combine(const uint16_t* out, int64_t rows_total, int32_t H,
             }
             y[t * (int64_t)H + c] = oracle_half_from_double((double)s);
         }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Router — "MetaX-TileLang工具链" §2.4: logits = W_g(x), scores =            */
+/* softmax(logits), (topk_scores, topk_indices) = topk(scores)                */
+/* ------------------------------------------------------------------------- */
+
+/* For every token t: logits[e] = sum_h x[t,h] * wg[e,h] in fp32 (natural h
+ * order); softmax over all E experts in fp32 (max subtracted, expf, sum in e
+ * order); the k largest logits (equal logits: the lower expert index first),
+ * in descending order; their probabilities are the routed weights.  The
+ * top-k is decided on the logits, which orders the experts exactly as the
+ * probabilities do.  Returns 0, or -1 for bad arguments. */
+int oracle_router(const uint16_t* x, int64_t n_tokens, int32_t H, const uint16_t* wg, int32_t E,
+                  int32_t top_k, int32_t* topk_ids, float* topk_weights, int32_t n_threads)
+{
+    if (!x || !wg || !topk_ids || !topk_weights || H <= 0 || E <= 0 || top_k <= 0 || top_k > E)
+        return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int64_t t;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (t = 0; t < n_tokens; ++t) {
+        float* logit = (float*)malloc(sizeof(float) * (size_t)E);
+        unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+        const uint16_t* xr = x + t * (int64_t)H;
+        for (int32_t e = 0; e < E; ++e) {
+            float acc = 0.0f;
+            for (int32_t h = 0; h < H; ++h)
+                acc += h2f(xr[h]) * h2f(wg[(int64_t)e * H + h]);
+            logit[e] = acc;
+        }
+        float mx = logit[0];
+        for (int32_t e = 1; e < E; ++e)
+            if (logit[e] > mx) mx = logit[e];
+        float sum = 0.0f;
+        for (int32_t e = 0; e < E; ++e) sum += expf(logit[e] - mx);
+        for (int32_t j = 0; j < top_k; ++j) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || logit[e] > logit[best])) best = e;
+            taken[best] = 1;
+            topk_ids[t * top_k + j] = best;
+            topk_weights[t * top_k + j] = expf(logit[best] - mx) / sum;
+        }
+        free(logit);
+        free(taken);
     }
     return 0;
 }

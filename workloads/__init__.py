@@ -25,7 +25,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "routing", "tokens", "expert_weights"]
+__all__ = ["Workload", "WORKLOADS", "routing", "tokens", "expert_weights", "router_weights"]
 
 
 @dataclass(frozen=True)
@@ -118,3 +118,10 @@ def expert_weights(w: Workload, seed: int = 0, device: str = "cpu", experts=None
     up = draw((E, w.intermediate, w.hidden), su)
     down = draw((E, w.hidden, w.intermediate), sd)
     return gate, up, down
+
+
+def router_weights(w: Workload, seed: int = 0) -> np.ndarray:
+    """Router weight W_g [E, H] ~ N(0, 1/H), fp16 (numpy, host)."""
+    rng = np.random.default_rng(seed + 2_000_003)
+    return (rng.standard_normal((w.experts, w.hidden), dtype=np.float32)
+            / np.float32(np.sqrt(w.hidden))).astype(np.float16)
