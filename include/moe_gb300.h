@@ -173,6 +173,25 @@ moe_status_t moe_combine_routed(const uint16_t* out, int64_t total_padded_tokens
                                 const int32_t* pair_padded_rows, int64_t n_tokens, int32_t top_k,
                                 uint16_t* y, void* stream);
 
+#define MOE_ROUTER_MAX_EXPERTS 256
+#define MOE_ROUTER_MAX_TOPK    16
+
+/* Router ("MetaX-TileLang工具链", §2.4: logits = W_g(x), scores =
+ * softmax(logits), topk_scores, topk_indices = topk(scores)).
+ *   x_tokens      [n_tokens, hidden] fp16
+ *   router_w      [n_experts, hidden] fp16 (W_g; a logit is a row of W_g
+ *                 dotted with the token, accumulated in fp32)
+ *   topk_ids      out: [n_tokens, top_k] int32, the top_k experts by logit in
+ *                 descending order; equal logits: the lower expert index first
+ *   topk_weights  out: [n_tokens, top_k] fp32, their softmax probabilities over
+ *                 all n_experts (not renormalised over the k)
+ * Limits: hidden % 128 == 0, n_experts <= MOE_ROUTER_MAX_EXPERTS, top_k <=
+ * min(n_experts, MOE_ROUTER_MAX_TOPK).  One kernel launch (a tcgen05 MMA tile
+ * of 128 tokens x all experts per CTA, softmax and top-k in its epilogue). */
+moe_status_t moe_router_topk(const uint16_t* x_tokens, int64_t n_tokens, int32_t hidden,
+                             const uint16_t* router_w, int32_t n_experts, int32_t top_k,
+                             int32_t* topk_ids, float* topk_weights, int32_t* status_dev, void* stream);
+
 /* Flags of moe_fused_forward_ex. */
 #define MOE_RUN_PHASE1   0x1u  /* gate+up GEMM and SiLU·up epilogue into up_logits   */
 #define MOE_RUN_PHASE2   0x2u  /* down GEMM and routed-weight epilogue into out       */

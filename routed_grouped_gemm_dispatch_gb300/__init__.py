@@ -17,6 +17,7 @@ Calls (names follow "Fused MoE GEMM æäº¤è¯´æ˜Ž", Â§æäº¤æ–‡ä»¶ / Â§å®Œæ•´ç®—å
                                                 a cached workspace is used)
   pack_routed(topk_ids, topk_weights, x_tokens, tables)  -> grouped, padded inputs
   combine_routed(out, pair_rows)                -> token-major sum of the expert rows
+  router_topk(x_tokens, router_w, top_k)        -> topk_ids, topk_weights
 """
 from __future__ import annotations
 
@@ -88,6 +89,8 @@ def lib():
         L.moe_pack_routed.restype = i32
         L.moe_combine_routed.argtypes = [P, i64, i32, P, i64, i32, P, P]
         L.moe_combine_routed.restype = i32
+        L.moe_router_topk.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
+        L.moe_router_topk.restype = i32
         _lib = L
         return L
 
@@ -270,6 +273,27 @@ def combine_routed(out, pair_rows, y=None, stream=None):
                                   _stream(stream))
     _check(st, "moe_combine_routed")
     return y
+
+
+def router_topk(x_tokens, router_w, top_k: int, topk_ids=None, topk_weights=None,
+                status=None, stream=None):
+    """Router logits (xÂ·W_gáµ€), softmax over all experts, top-k: returns
+    (topk_ids int32 [T, k], topk_weights fp32 [T, k])."""
+    import torch
+    x = _dev(x_tokens, "x_tokens", torch.float16, 2)
+    w = _dev(router_w, "router_w", torch.float16, 2)
+    T, H = x.shape
+    E = w.shape[0]
+    if w.shape[1] != H:
+        raise ValueError("router_w must be [n_experts, hidden]")
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    st = lib().moe_router_topk(_ptr(x), T, H, _ptr(w), E, int(top_k), _ptr(topk_ids),
+                               _ptr(topk_weights), _ptr(status), _stream(stream))
+    _check(st, "moe_router_topk")
+    return topk_ids, topk_weights
 
 
 _WORKSPACE = {}

@@ -124,6 +124,20 @@ moe_status_t moe_combine_routed(const uint16_t* out, int64_t total_padded_tokens
                                          static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_router_topk(const uint16_t* x_tokens, int64_t n_tokens, int32_t hidden,
+                             const uint16_t* router_w, int32_t n_experts, int32_t top_k, int32_t* topk_ids,
+                             float* topk_weights, int32_t* status_dev, void* stream) {
+    if (n_tokens < 0 || hidden <= 0 || hidden % 128 != 0) return MOE_ERR_SHAPE;
+    if (n_experts <= 0 || n_experts > MOE_ROUTER_MAX_EXPERTS) return MOE_ERR_LIMIT;
+    if (top_k <= 0 || top_k > n_experts || top_k > MOE_ROUTER_MAX_TOPK) return MOE_ERR_LIMIT;
+    if (n_tokens == 0) return MOE_OK;
+    if (!x_tokens || !router_w || !topk_ids || !topk_weights) return MOE_ERR_NULL;
+    if (!aligned16(x_tokens) || !aligned16(router_w)) return MOE_ERR_ALIGN;
+    if (moe_status_t s = check_device()) return s;
+    return from_cuda(moe::launch_router(x_tokens, n_tokens, hidden, router_w, n_experts, top_k, topk_ids,
+                                        topk_weights, status_dev, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,
                                   int32_t hidden, const uint16_t* gate_w, const uint16_t* up_w,
                                   const uint16_t* down_w, int32_t n_experts, int32_t intermediate,

@@ -48,6 +48,11 @@ cudaError_t launch_pack(const int32_t* topk_ids, const float* topk_weights, int6
 cudaError_t launch_combine(const uint16_t* out, int64_t rows_total, int32_t hidden, const int32_t* pair_rows,
                            int64_t n_tokens, int32_t top_k, uint16_t* y, cudaStream_t stream);
 
+// Router: logits, softmax, top-k.
+cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, const uint16_t* router_w,
+                          int32_t n_experts, int32_t top_k, int32_t* topk_ids, float* topk_weights,
+                          int32_t* status, cudaStream_t stream);
+
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 

@@ -1,0 +1,270 @@
+// Router: logits = x · W_gᵀ (fp32), softmax over all experts, top-k
+// ("MetaX-TileLang工具链", §2.4: logits = W_g(x), scores = softmax(logits),
+// topk_scores, topk_indices = topk(scores)).
+//
+// One CTA per 128-token tile, one tcgen05 MMA tile of M = 128 tokens and
+// N = n_experts rounded up to 16 (at most 256), so a token's whole logit row
+// sits in one TMEM lane.  Warp 0 streams x and W_g with TMA (4 stages of
+// 64-wide K), warp 1 owns TMEM and issues the MMAs, warps 2-5 each take 32
+// tokens: an online softmax (running max and rescaled sum) and a register
+// top-k over the row, ties to the lower expert index, written in descending
+// order.  The top-k is decided on the logits (softmax preserves their order).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/moe_gb300.h"
+#include "moe_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int R_BM = 128;
+constexpr int R_BK = 64;
+constexpr int R_STAGES = 4;
+constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB
+constexpr int R_B_MAX_BYTES = 256 * R_BK * 2;        // 32 KB
+constexpr int R_STAGE_BYTES = R_A_BYTES + R_B_MAX_BYTES;
+constexpr int R_THREADS = 192;
+constexpr int R_EPI_THREADS = 128;
+constexpr int R_MAX_TOPK = 16;
+constexpr uint64_t R_WAIT_NS = 2000000000ull;
+constexpr uint64_t R_DRAIN_NS = 200000000ull;
+constexpr int R_OFF_BARS = R_STAGES * R_STAGE_BYTES;
+constexpr int R_OFF_TMEM = R_OFF_BARS + (2 * R_STAGES + 2) * 8;
+constexpr int R_OFF_ABORT = R_OFF_TMEM + 4;
+constexpr size_t R_SMEM = 1024 + R_OFF_ABORT + 16;
+
+struct RouterParams {
+    int64_t n_tokens;
+    int32_t n_experts;
+    int32_t n_pad;         // n_experts rounded up to 16
+    int32_t tmem_cols;     // power of two >= max(32, n_pad)
+    int32_t top_k;
+    int32_t k_blocks;      // hidden / 64
+    int32_t* topk_ids;
+    float* topk_weights;
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(R_THREADS, 1)
+router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+              const RouterParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + R_OFF_BARS;
+    const uint32_t bar_empty = bar_full + 8 * R_STAGES;
+    const uint32_t bar_tfull = bar_empty + 8 * R_STAGES;
+    const uint32_t bar_drain = bar_tfull + 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + R_OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + R_OFF_ABORT);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t b_bytes = static_cast<uint32_t>(p.n_pad) * R_BK * 2;
+
+    if (tid == 0) {
+        for (int s = 0; s < R_STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_x);
+        tma_prefetch_map(&map_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + R_OFF_TMEM, static_cast<uint32_t>(p.tmem_cols));
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const int32_t row0 = static_cast<int32_t>(blockIdx.x) * R_BM;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_normal();
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, R_WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_full + 8 * stage;
+                const uint32_t sa = sbase + stage * R_STAGE_BYTES;
+                mbar_arrive_expect_tx(fb, R_A_BYTES + b_bytes);
+                tma_load_2d(sa, &map_x, fb, kb * R_BK, row0, pol);
+                tma_load_2d(sa + R_A_BYTES, &map_w, fb, kb * R_BK, 0, pol);
+                ++issued;
+                if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) {
+                volatile int never = 0;
+                const int64_t n = issued < R_STAGES ? issued : R_STAGES;
+                for (int64_t i = 0; i < n; ++i) {
+                    const int64_t idx = issued - 1 - i;
+                    mbar_wait_bounded(bar_full + 8 * static_cast<uint32_t>(idx % R_STAGES),
+                                      static_cast<uint32_t>((idx / R_STAGES) & 1), &never, R_DRAIN_NS);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32acc(R_BM, static_cast<uint32_t>(p.n_pad));
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, R_WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = sbase + stage * R_STAGE_BYTES;
+                const uint32_t sb = sa + R_A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < R_BK / 16; ++kk)
+                    tc_mma_f16(tmem_base, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32), idesc,
+                               (kb | kk) != 0 ? 1u : 0u);
+                tc_commit(bar_empty + 8 * stage);
+                if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (ok) tc_commit(bar_tfull);
+            volatile int never = 0;
+            tc_commit(bar_drain);
+            mbar_wait_bounded(bar_drain, 0, &never, R_DRAIN_NS);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int64_t t = static_cast<int64_t>(row0) + row;
+        if (mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS)) {
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            float m = -INFINITY, s = 0.0f;
+            float best_v[R_MAX_TOPK];
+            int32_t best_i[R_MAX_TOPK];
+            for (int j = 0; j < R_MAX_TOPK; ++j) {
+                best_v[j] = -INFINITY;
+                best_i[j] = -1;
+            }
+            for (int32_t c0 = 0; c0 < p.n_pad; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + c0, v);
+                tmem_ld_wait();
+                for (int j = 0; j < 32; ++j) {
+                    const int32_t e = c0 + j;
+                    if (e >= p.n_experts) break;
+                    const float l = __uint_as_float(v[j]);
+                    if (l > m) {
+                        s = s * expf(m - l) + 1.0f;
+                        m = l;
+                    } else {
+                        s += expf(l - m);
+                    }
+                    // insert after any equal value: equal logits keep the lower index first
+                    if (best_i[p.top_k - 1] < 0 || l > best_v[p.top_k - 1]) {
+                        int32_t pos = p.top_k - 1;
+                        while (pos > 0 && (best_i[pos - 1] < 0 || l > best_v[pos - 1])) {
+                            best_v[pos] = best_v[pos - 1];
+                            best_i[pos] = best_i[pos - 1];
+                            --pos;
+                        }
+                        best_v[pos] = l;
+                        best_i[pos] = e;
+                    }
+                }
+            }
+            if (t < p.n_tokens) {
+                for (int j = 0; j < p.top_k; ++j) {
+                    p.topk_ids[t * p.top_k + j] = best_i[j];
+                    p.topk_weights[t * p.top_k + j] = expf(best_v[j] - m) / s;
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn router_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    });
+    return fn;
+}
+
+bool router_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {R_BK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return router_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, const uint16_t* router_w,
+                          int32_t n_experts, int32_t top_k, int32_t* topk_ids, float* topk_weights,
+                          int32_t* status, cudaStream_t stream) {
+    if (n_tokens == 0) return cudaSuccess;
+    if (!router_encode_fn()) return cudaErrorNotSupported;
+    RouterParams p{};
+    p.n_tokens = n_tokens;
+    p.n_experts = n_experts;
+    p.n_pad = ((n_experts + 15) / 16) * 16;
+    int cols = 32;
+    while (cols < p.n_pad) cols <<= 1;
+    p.tmem_cols = cols;
+    p.top_k = top_k;
+    p.k_blocks = hidden / R_BK;
+    p.topk_ids = topk_ids;
+    p.topk_weights = topk_weights;
+    p.status = status;
+    CUtensorMap map_x, map_w;
+    if (!router_map(&map_x, x, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(hidden), R_BM) ||
+        !router_map(&map_w, router_w, static_cast<uint64_t>(n_experts), static_cast<uint64_t>(hidden),
+                    static_cast<uint32_t>(p.n_pad)))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(R_SMEM));
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>((n_tokens + R_BM - 1) / R_BM);
+    router_kernel<<<grid, R_THREADS, R_SMEM, stream>>>(map_x, map_w, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
