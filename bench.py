@@ -437,6 +437,64 @@ def main():
                "path": "pinned host tokens [T,H] + topk_ids + topk weights -> H2D -> moe_build_dispatch -> "
                        "moe_pack_routed -> moe_fused_forward -> moe_combine_routed -> D2H token outputs [T,H]"}
 
+    # ---- timing scopes of the evaluation page: the whole MoE layer ---------
+    # cached_e2e: router -> dispatch -> pack -> forward -> combine on tokens
+    # already on the device, all buffers reused (routing from a random router,
+    # so it is near-uniform whatever the workload's own routing is);
+    # e2e_host: the same with the tokens copied in and the outputs copied out.
+    scopes = None
+    if not args.no_e2e:
+        wg = torch.from_numpy(workloads.router_weights(w, args.seed + rank)).to(dev)
+        ids_l = torch.empty_like(d["ids"])
+        tw_l = torch.empty_like(d["tw"])
+        prows_l = torch.empty((w.tokens, w.top_k), dtype=torch.int32, device=dev)
+        ws_l = torch.empty(max(16, int(moe.lib().moe_pack_workspace_bytes(w.pairs, E))), dtype=torch.uint8,
+                           device=dev)
+        y_l = torch.empty((w.tokens, w.hidden), dtype=torch.float16, device=dev)
+        h_xl = d["x_tok"].cpu().pin_memory()
+        h_yl = torch.empty((w.tokens, w.hidden), dtype=torch.float16).pin_memory()
+        x_l = torch.empty_like(d["x_tok"])
+        x_l.copy_(d["x_tok"])
+        t_l = {key: torch.empty_like(val) for key, val in t.items()}   # the layer's own tables
+
+        def layer(x_in):
+            moe.router_topk(x_in, wg, w.top_k, topk_ids=ids_l, topk_weights=tw_l)
+            moe.build_dispatch(ids_l, E, out=t_l)
+            moe.pack_routed(ids_l, tw_l, x_in, t_l, d["rows_total"], stacked=d["xp"], routed_weights=d["rw"],
+                            pair_rows=prows_l, workspace=ws_l)
+            moe.fused_forward(d["xp"], d["gate"], d["up"], d["down"], d["rw"], t_l["group_sizes"],
+                              t_l["group_offsets"], t_l["group_padded_offsets"], t_l["group_idx_for_bx"],
+                              d["ul"], d["out"])
+            moe.combine_routed(d["out"], prows_l, y=y_l)
+
+        def layer_host():
+            x_l.copy_(h_xl, non_blocking=True)
+            layer(x_l)
+            h_yl.copy_(y_l, non_blocking=True)
+
+        def time_fn(fn, n):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(n):
+                fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / n
+
+        n_sc = max(5, min(args.steps, 100))
+        cached_ms = time_fn(lambda: layer(x_l), n_sc)
+        host_ms = time_fn(layer_host, n_sc)
+        router_flops = 2.0 * w.tokens * w.hidden * w.experts
+        scopes = {"routed_kernel_only_ms": ms, "cached_e2e_ms": cached_ms, "e2e_host_ms": host_ms,
+                  "cached_e2e_tflops": world * (flops + router_flops) / (cached_ms * 1e-3) / 1e12,
+                  "e2e_host_tflops": world * (flops + router_flops) / (host_ms * 1e-3) / 1e12,
+                  "flops_note": "expert FLOPs 6*P*H*I plus router 2*T*H*E; routing from a random "
+                                "router (near-uniform), not the workload's own routing",
+                  "launches_per_layer": 9}
+
     # ---- roofline --------------------------------------------------------------
     peaks, src = load_peaks()
     sizes = t["group_sizes"].cpu().numpy()
@@ -478,7 +536,7 @@ def main():
                 "config": config_of(w, "working set larger than L2 (no flush needed)"),
                 "parallelism": "replicas only" if world > 1 else "single GPU",
                 "roofline": roof, "forward_roofline": forward_roofline,
-                "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "cpu_baseline": cpu, "e2e": e2e, "scopes": scopes, "clocks": clocks,
                 "gpu_launches": 3 * args.steps, "device_status": dev_status,
                 "kernel_source_sha": kernel_source_hash()}
         print(json.dumps(line), flush=True)
