@@ -15,6 +15,7 @@
 
 #include "../../include/moe_gb300.h"
 #include "moe_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -41,6 +42,9 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     __shared__ int32_t wsum_p[DISPATCH_THREADS / 32];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // A forward launched right behind this kernel may start its own set-up
+    // now; it reads the tables only after this grid has completed.
+    pdl_launch_dependents();
     for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
     __syncthreads();
 

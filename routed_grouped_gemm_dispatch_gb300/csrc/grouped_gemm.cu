@@ -101,6 +101,8 @@ struct GemmParams {
     int32_t k_blocks;         // K / 64
     int32_t n_tiles;          // N slices per block
     int32_t n_extent;         // I (phase 1) or H (phase 2): columns of dst
+    int32_t tables_before_wait;  // phase 2 right behind phase 1: the tables may be read before
+                                 // waiting for phase 1 (phase 1 lets it start only after its own wait)
 };
 
 // Rows of block bx that belong to its expert ("Fused MoE GEMM 提交说明",
@@ -191,8 +193,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t rank = cluster_cta_rank();
     const bool leader = rank == 0;
 
-    if (PHASE == 1) pdl_launch_dependents();
-
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);           // the even CTA's arrive.expect_tx
@@ -216,6 +216,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         tmem_alloc_pair(sbase + OFF_TMEM_SLOT, TMEM_COLS);
         tmem_relinquish_pair();
     }
+
+    // Launched with programmatic dependent launch: everything above overlaps
+    // the previous kernel; every global read below comes after its completion.
+    // Phase 2 directly behind phase 1 may read the dispatch tables earlier
+    // (phase 1 only lets it start once phase 1 itself has waited).
+    if (PHASE == 1 || !p.tables_before_wait) pdl_wait_prior_grid();
+    if (PHASE == 1) pdl_launch_dependents();
 
     // ---- 1. compacted list of active blocks and their experts (bx order) ---
     int32_t nact = 0;
@@ -287,7 +294,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
     // Phase 2 reads up_logits written by phase 1: wait for that grid here
     // (everything above only touched the dispatch tables).
-    if (PHASE == 2) pdl_wait_prior_grid();
+    if (PHASE == 2 && p.tables_before_wait) pdl_wait_prior_grid();
 
     const int32_t cluster_id = static_cast<int32_t>(blockIdx.x) / CLUSTER;
     const int32_t n_clusters = static_cast<int32_t>(gridDim.x) / CLUSTER;
@@ -632,6 +639,7 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     p2.k_blocks = a.intermediate / (BK * KSUB);
     p2.n_tiles = (a.hidden + BN - 1) / BN;
     p2.n_extent = a.hidden;
+    p2.tables_before_wait = (flags & MOE_RUN_PHASE1) ? 1 : 0;
 
     const size_t smem = smem_bytes_for(a.num_blocks_m);
     cudaError_t err = cudaSuccess;
@@ -659,13 +667,14 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         const int nc = max_clusters<1>(smem);
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;   // cluster + programmatic dependent launch
         err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x16, map_gate, map_up, p1);
         if (err != cudaSuccess) return err;
     }
     if (flags & MOE_RUN_PHASE2) {
         // Phase 2 may start its prologue (tables, TMEM, barriers) while phase 1
-        // drains; it waits for phase 1's results before its first load.
+        // drains; it waits for phase 1's results before its first load.  Both
+        // phases are launched with programmatic dependent launch.
         const int nc = max_clusters<2>(smem);
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
