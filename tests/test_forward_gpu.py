@@ -15,7 +15,7 @@ import oracle
 import routed_grouped_gemm_dispatch_gb300 as moe
 import workloads
 from gpu_side import bits, gpu_prepare, run_forward
-from moe_cases import (BT, SENTINEL, oracle_prepare, raw_inputs, small_workload,
+from moe_cases import (BT, SENTINEL, Raw, oracle_prepare, raw_inputs, small_workload,
                        within_tol)
 
 pytestmark = pytest.mark.gpu
@@ -174,3 +174,50 @@ def test_full_size_sampled_rows(name):
     ok_o = within_tol(out_g[rows], out_r, ATOL, RTOL)
     assert ok_u.all(), f"{np.count_nonzero(~ok_u)} up_logits entries outside tolerance"
     assert ok_o.all(), f"{np.count_nonzero(~ok_o)} out entries outside tolerance"
+
+
+def test_dsv3_full_size_sampled_rows():
+    """DeepSeek-V3-shaped (22.5 GB of expert weights, drawn on the GPU): the
+    oracle recomputes sampled valid rows; it gets host copies of only the
+    sampled rows' experts (the other experts' slices stay unread zeros)."""
+    w = workloads.WORKLOADS["dsv3"]
+    ids, tw = workloads.routing(w, seed=0)
+    x = workloads.tokens(w, seed=0)
+    gate, up, down = workloads.expert_weights(w, seed=0, device="cuda")
+    raw = Raw(w, ids, tw, x, None, None, None)
+    side_g = gpu_prepare(raw, weights=(gate, up, down))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ul, out = run_forward(side_g, w.intermediate, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+    tab = oracle.build_dispatch(ids, w.experts)
+    for key in ("group_sizes", "group_offsets", "group_padded_offsets", "group_idx_for_bx"):
+        assert np.array_equal(side_g.tables[key].cpu().numpy(), tab[key])
+    prow = oracle.pair_padded_rows(ids, w.experts, tab["group_padded_offsets"])
+    assert np.array_equal(side_g.pair_rows.cpu().numpy(), prow)
+    rows_total = tab["num_blocks_m"] * BT
+    xo, rwo = oracle.pack(x, ids, tw, prow, tab, rows_total)
+    rows = _sample_rows(prow, tab, np.random.default_rng(1), n_random=16)
+    experts = sorted({int(tab["group_idx_for_bx"][r // BT]) for r in rows})
+    E, I, H = w.experts, w.intermediate, w.hidden
+    g_np = np.zeros((E, I, H), np.float16)
+    u_np = np.zeros((E, I, H), np.float16)
+    d_np = np.zeros((E, H, I), np.float16)
+    for e in experts:
+        g_np[e] = gate[e].cpu().numpy()
+        u_np[e] = up[e].cpu().numpy()
+        d_np[e] = down[e].cpu().numpy()
+    up_r, out_r, valid = oracle.forward_rows(xo, g_np, u_np, d_np, rwo, tab, rows)
+    assert valid.all()
+    up_g = ul.view(torch.int16)[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16)
+    out_g = out.view(torch.int16)[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16)
+    ok_u = within_tol(up_g, up_r, ATOL, RTOL)
+    ok_o = within_tol(out_g, out_r, ATOL, RTOL)
+    assert ok_u.all(), f"{np.count_nonzero(~ok_u)} up_logits entries outside tolerance"
+    assert ok_o.all(), f"{np.count_nonzero(~ok_o)} out entries outside tolerance"
+    # every padding row of out is untouched (checked on the device)
+    valid_mask = torch.zeros(rows_total, dtype=torch.bool, device="cuda")
+    valid_mask[side_g.pair_rows.reshape(-1).long()] = True
+    pad_rows = out.view(torch.int16)[~valid_mask]
+    assert bool((pad_rows == SENTINEL).all())
