@@ -214,6 +214,31 @@ moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t
                                   uint16_t* up_logits, uint16_t* out,
                                   int32_t* status_dev, void* stream, uint32_t flags);
 
+/* Workspace bytes of moe_fused_forward_single_launch (one int32 counter per
+ * 128-row block, rounded up).  Returns -1 for a negative argument. */
+int64_t moe_single_launch_workspace_bytes(int64_t num_blocks_m);
+
+/* moe_fused_forward with both phases in ONE persistent launch (same
+ * arguments, results and errors, plus a workspace).  Each cluster of two CTAs
+ * runs its phase-1 tiles, then its phase-2 tiles; a phase-2 tile of a unit of
+ * blocks starts as soon as every phase-1 tile of that unit has stored its
+ * up_logits rows (per-unit counters in `workspace`, zeroed by this call with a
+ * cudaMemsetAsync on `stream`), so the phase-1 tail and the kernel boundary
+ * overlap phase-2 work.  The waits are bounded (MOE_DEV_TIMEOUT) and need all
+ * clusters of the launch resident at once, which the grid size ensures when
+ * no other kernel holds SMs for long.  Workspace: device memory of
+ * moe_single_launch_workspace_bytes(num_blocks_m) bytes, caller-owned; calls
+ * that overlap on the GPU must not share it. */
+moe_status_t moe_fused_forward_single_launch(
+    const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens, int32_t hidden,
+    const uint16_t* gate_w, const uint16_t* up_w, const uint16_t* down_w,
+    int32_t n_experts, int32_t intermediate,
+    const float* routed_expert_weights, int64_t total_valid_tokens,
+    const int32_t* group_sizes, const int32_t* group_offsets,
+    const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx, int64_t num_blocks_m,
+    uint16_t* up_logits, uint16_t* out, void* workspace, size_t workspace_bytes,
+    int32_t* status_dev, void* stream);
+
 /* Size of the fixed workspace used by moe_fused_forward_static_workspace. */
 #define MOE_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 

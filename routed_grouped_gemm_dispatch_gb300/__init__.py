@@ -91,8 +91,17 @@ def lib():
         L.moe_combine_routed.restype = i32
         L.moe_router_topk.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
         L.moe_router_topk.restype = i32
+        L.moe_single_launch_workspace_bytes.argtypes = [i64]
+        L.moe_single_launch_workspace_bytes.restype = i64
+        L.moe_fused_forward_single_launch.argtypes = [P, i64, i32, P, P, P, i32, i32, P, i64,
+                                                      P, P, P, P, i64, P, P, P, ctypes.c_size_t, P, P]
+        L.moe_fused_forward_single_launch.restype = i32
         _lib = L
         return L
+
+
+def single_launch_workspace_bytes(num_blocks_m: int) -> int:
+    return int(lib().moe_single_launch_workspace_bytes(int(num_blocks_m)))
 
 
 def status_string(status: int) -> str:
@@ -163,10 +172,12 @@ def build_dispatch(topk_ids, n_experts: int, block_token: int = BLOCK_TOKEN,
 def fused_forward(stacked_expert_tokens, gate_w, up_w, down_w, routed_expert_weights,
                   group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
                   up_logits, out, status=None, stream=None,
-                  flags: int = MOE_RUN_PHASE1 | MOE_RUN_PHASE2):
+                  flags: int = MOE_RUN_PHASE1 | MOE_RUN_PHASE2, single_launch_workspace=None):
     """Phase 1 + phase 2 on the current stream; writes ``up_logits`` and ``out``
     in place on valid rows only.  ``flags`` selects phases (MOE_RUN_PHASE1 /
-    MOE_RUN_PHASE2, optionally MOE_NO_PDL)."""
+    MOE_RUN_PHASE2, optionally MOE_NO_PDL).  With ``single_launch_workspace``
+    (a device tensor of at least single_launch_workspace_bytes() bytes) both
+    phases run in one persistent launch."""
     import torch
     x = _dev(stacked_expert_tokens, "stacked_expert_tokens", torch.float16, 2)
     g = _dev(gate_w, "gate_w", torch.float16, 3)
@@ -190,7 +201,11 @@ def fused_forward(stacked_expert_tokens, gate_w, up_w, down_w, routed_expert_wei
     args = (_ptr(x), rows, H, _ptr(g), _ptr(u), _ptr(d), E, I, _ptr(rw), rw.numel(),
             _ptr(sizes), _ptr(offs), _ptr(padded), _ptr(gidx), gidx.numel(),
             _ptr(ul), _ptr(o), _ptr(status), _stream(stream))
-    if flags == (MOE_RUN_PHASE1 | MOE_RUN_PHASE2):
+    if single_launch_workspace is not None:
+        ws = single_launch_workspace
+        _check(lib().moe_fused_forward_single_launch(*args[:17], _ptr(ws), ws.numel() * ws.element_size(),
+                                                     *args[17:]), "moe_fused_forward_single_launch")
+    elif flags == (MOE_RUN_PHASE1 | MOE_RUN_PHASE2):
         _check(lib().moe_fused_forward(*args), "moe_fused_forward")
     else:
         _check(lib().moe_fused_forward_ex(*args, int(flags)), "moe_fused_forward_ex")

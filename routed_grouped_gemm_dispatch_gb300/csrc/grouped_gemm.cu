@@ -86,23 +86,29 @@ constexpr int OFF_UNITS = ((OFF_WSUM + (NUM_THREADS / 32) * 4 + 15) / 16) * 16;
 __host__ __device__ inline size_t units_bytes(int64_t m) { return ((2 * static_cast<size_t>(m) + 15) / 16) * 16; }
 size_t smem_bytes_for(int64_t m) { return 1024 /* alignment slack */ + OFF_UNITS + units_bytes(m); }
 
+struct PhaseParams {
+    uint16_t* dst;            // up_logits (phase 1) or out (phase 2)
+    int32_t k_blocks;         // K / (64 * KSUB)
+    int32_t n_tiles;          // N slices per block
+    int32_t n_extent;         // I (phase 1) or H (phase 2): columns of dst
+};
+
 struct GemmParams {
     const int32_t* sizes;
     const int32_t* offsets;
     const int32_t* padded;
     const int32_t* gidx;
     const float* rw;          // phase 2 only
-    uint16_t* dst;            // up_logits (phase 1) or out (phase 2)
     int32_t* status;
     int64_t rows_total;
     int64_t valid_total;
     int32_t num_blocks_m;
     int32_t n_experts;
-    int32_t k_blocks;         // K / 64
-    int32_t n_tiles;          // N slices per block
-    int32_t n_extent;         // I (phase 1) or H (phase 2): columns of dst
+    PhaseParams ph[2];        // [0]: phase 1 (gate+up), [1]: phase 2 (down)
     int32_t tables_before_wait;  // phase 2 right behind phase 1: the tables may be read before
                                  // waiting for phase 1 (phase 1 lets it start only after its own wait)
+    int32_t* ready;           // both phases in one launch: per unit, finished phase-1 tile stores
+                              // (zero at launch)
 };
 
 // Rows of block bx that belong to its expert ("Fused MoE GEMM 提交说明",
@@ -159,15 +165,55 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// map_a / map_a16: activations (x or up_logits), boxes of 64 x 128 and 64 x 16
-// rows; map_b0 / map_b1: phase 1 gate / up (box 64 x 128), phase 2 down (box
-// 64 x 128, map_b1 unused).
+// Which phase a tile of the launch belongs to, and its index inside that
+// phase.  PHASE 1 or 2 launches run one phase; PHASE 3 runs both: the first
+// nunits * n_tiles(phase 1) tiles are phase 1, the rest phase 2.
+struct PhaseTile {
+    int ph;
+    int32_t t;
+};
+
+template <int PHASE>
+__device__ __forceinline__ PhaseTile phase_of(int32_t t, int32_t tiles1) {
+    if (PHASE == 1) return PhaseTile{1, t};
+    if (PHASE == 2) return PhaseTile{2, t};
+    return t < tiles1 ? PhaseTile{1, t} : PhaseTile{2, t - tiles1};
+}
+
+// Wait (bounded) until *counter >= need, with acquire ordering.
+__device__ __forceinline__ bool counter_wait_bounded(const int32_t* counter, int32_t need, volatile int* abort,
+                                                     uint64_t limit_ns) {
+    auto load = [&]() {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+        return v;
+    };
+    if (load() >= need) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (load() >= need) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// map_x / map_x16: x (boxes 64 x 128 and 64 x 16 rows); map_gate / map_up:
+// phase-1 weights (box 64 x 128); map_u / map_u16: up_logits; map_down:
+// phase-2 weights (box 64 x 128).  A launch of one phase gets placeholders for
+// the other phase's maps.
 template <int PHASE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_a16,
-                    const __grid_constant__ CUtensorMap map_b0,
-                    const __grid_constant__ CUtensorMap map_b1,
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
+                    const __grid_constant__ CUtensorMap map_x16,
+                    const __grid_constant__ CUtensorMap map_gate,
+                    const __grid_constant__ CUtensorMap map_up,
+                    const __grid_constant__ CUtensorMap map_u,
+                    const __grid_constant__ CUtensorMap map_u16,
+                    const __grid_constant__ CUtensorMap map_down,
                     const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -207,10 +253,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&map_a);
-        tma_prefetch_map(&map_a16);
-        tma_prefetch_map(&map_b0);
-        if (PHASE == 1) tma_prefetch_map(&map_b1);
+        if (PHASE != 2) {
+            tma_prefetch_map(&map_x);
+            tma_prefetch_map(&map_x16);
+            tma_prefetch_map(&map_gate);
+            tma_prefetch_map(&map_up);
+        }
+        if (PHASE != 1) {
+            tma_prefetch_map(&map_u);
+            tma_prefetch_map(&map_u16);
+            tma_prefetch_map(&map_down);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(sbase + OFF_TMEM_SLOT, TMEM_COLS);
@@ -221,7 +274,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // the previous kernel; every global read below comes after its completion.
     // Phase 2 directly behind phase 1 may read the dispatch tables earlier
     // (phase 1 only lets it start once phase 1 itself has waited).
-    if (PHASE == 1 || !p.tables_before_wait) pdl_wait_prior_grid();
+    if (PHASE != 2 || !p.tables_before_wait) pdl_wait_prior_grid();
     if (PHASE == 1) pdl_launch_dependents();
 
     // ---- 1. compacted list of active blocks and their experts (bx order) ---
@@ -283,7 +336,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int32_t total_tiles = counts[1] * p.n_tiles;
+    const int32_t tiles1 = PHASE == 2 ? 0 : counts[1] * p.ph[0].n_tiles;
+    const int32_t total_tiles = PHASE == 1 ? tiles1
+                              : PHASE == 2 ? counts[1] * p.ph[1].n_tiles
+                                           : tiles1 + counts[1] * p.ph[1].n_tiles;
     // With about one unit per expert run every weight byte is used once:
     // stream the weights through L2 with evict-first; otherwise keep them for
     // the expert's other units.
@@ -313,14 +369,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             // t + 2C and that expert's size and padded offset for tile t + C
             // are loaded while tile t streams (C = number of clusters).
             auto expert_of = [&](int32_t tt) -> int32_t {
-                return tt < total_tiles ? __ldg(p.gidx + decode_tile(tt, units, p.n_tiles, rank).bx0) : 0;
+                if (tt >= total_tiles) return 0;
+                const PhaseTile pt = phase_of<PHASE>(tt, tiles1);
+                return __ldg(p.gidx + decode_tile(pt.t, units, p.ph[pt.ph - 1].n_tiles, rank).bx0);
             };
             int32_t e_cur = expert_of(cluster_id);
             int32_t size_cur = __ldg(p.sizes + e_cur), pad_cur = __ldg(p.padded + e_cur);
             int32_t e_next = expert_of(cluster_id + n_clusters);
             for (int32_t t = cluster_id; t < total_tiles && ok; t += n_clusters) {
-                const Tile ti = decode_tile(t, units, p.n_tiles, rank);
+                const PhaseTile pt = phase_of<PHASE>(t, tiles1);
+                const PhaseParams& pp = p.ph[pt.ph - 1];
+                const Tile ti = decode_tile(pt.t, units, pp.n_tiles, rank);
                 const int32_t e = e_cur;
+                const CUtensorMap* a_map = pt.ph == 1 ? &map_x : &map_u;
+                const CUtensorMap* a16_map = pt.ph == 1 ? &map_x16 : &map_u16;
+                if (PHASE == 3 && pt.ph == 2) {
+                    // this tile reads the unit's up_logits rows: wait until every
+                    // phase-1 tile of the unit has stored them (both CTAs for a
+                    // pair, the even CTA for a single), then order those generic
+                    // stores before this thread's TMA (async proxy) reads
+                    const int32_t u = pt.t / pp.n_tiles;
+                    const int32_t need = p.ph[0].n_tiles * (ti.pair ? 2 : 1);
+                    if (!counter_wait_bounded(p.ready + u, need, abort_flag, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 const int32_t size_next = __ldg(p.sizes + e_next), pad_next = __ldg(p.padded + e_next);
                 const int32_t e_next2 = expert_of(t + 2 * n_clusters);
                 // Rows of A to load: none for the odd CTA of a single block
@@ -343,7 +418,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 const uint32_t bytes_peer = (leader && ti.pair) ? a_bytes(a_boxes(ti.bx0 + 1)) : 0;
                 const uint32_t stage_tx =
                     KSUB * ((load_a ? a_bytes(boxes_own) : 0) + bytes_peer + 2 * B_BOX_BYTES);
-                for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                for (int32_t kb = 0; kb < pp.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
@@ -356,17 +431,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     for (int ks = 0; ks < KSUB; ++ks) {
                         const int32_t k0 = (kb * KSUB + ks) * BK;
                         if (load_a && boxes_own == 0) {
-                            tma_load_2d_pair(sa + ks * A_BOX_BYTES, &map_a, fb, k0, ti.bx * BM, pol_a);
+                            tma_load_2d_pair(sa + ks * A_BOX_BYTES, a_map, fb, k0, ti.bx * BM, pol_a);
                         } else if (load_a) {
                             for (int32_t b = 0; b < boxes_own; ++b)
-                                tma_load_2d_pair(sa + ks * A_BOX_BYTES + b * (A_BOX_BYTES / 8), &map_a16, fb, k0,
+                                tma_load_2d_pair(sa + ks * A_BOX_BYTES + b * (A_BOX_BYTES / 8), a16_map, fb, k0,
                                                  ti.bx * BM + b * 16, pol_a);
                         }
-                        if (PHASE == 1)
-                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, leader ? &map_b0 : &map_b1, fb, k0, ti.n * 128,
-                                             e, pol_b);
+                        if (pt.ph == 1)
+                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, leader ? &map_gate : &map_up, fb, k0,
+                                             ti.n * 128, e, pol_b);
                         else
-                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, &map_b0, fb, k0,
+                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, &map_down, fb, k0,
                                              ti.n * BN + static_cast<int32_t>(rank) * 128, e, pol_b);
                     }
                     ++issued;
@@ -408,7 +483,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+                const int32_t k_blocks = p.ph[phase_of<PHASE>(t, tiles1).ph - 1].k_blocks;
+                for (int32_t kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
@@ -445,15 +521,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         const uint32_t leader_tempty = mapa_shared(bar_tempty, 0);
         uint32_t acc = 0, aphase = 0;
         for (int32_t t = cluster_id; t < total_tiles; t += n_clusters) {
-            const Tile ti = decode_tile(t, units, p.n_tiles, rank);
+            const PhaseTile pt = phase_of<PHASE>(t, tiles1);
+            const PhaseParams& pp = p.ph[pt.ph - 1];
+            const Tile ti = decode_tile(pt.t, units, pp.n_tiles, rank);
             int32_t e = 0, tok = 0;
             const int32_t actual = ti.store ? block_rows(p, ti.bx, &e, &tok) : 0;
             if (!mbar_wait_bounded(bar_tfull + 8 * acc, aphase, abort_flag, WAIT_LIMIT_NS)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
             const int64_t grow = static_cast<int64_t>(ti.bx) * BM + row;
-            if (PHASE == 1) {
-                uint16_t* dst_row = p.dst + grow * p.n_extent + static_cast<int64_t>(ti.n) * 128;
+            if (pt.ph == 1) {
+                uint16_t* dst_row = pp.dst + grow * pp.n_extent + static_cast<int64_t>(ti.n) * 128;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t g[32], u[32];
@@ -480,11 +558,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             } else {
                 float w = 0.0f;
                 if (row < actual) w = __ldg(p.rw + (__ldg(p.offsets + e) + tok + row));
-                uint16_t* dst_row = p.dst + grow * p.n_extent;
+                uint16_t* dst_row = pp.dst + grow * pp.n_extent;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     const int32_t col0 = ti.n * BN + c * 32;
-                    if (col0 >= p.n_extent) break;              // partial last slice of H
+                    if (col0 >= pp.n_extent) break;             // partial last slice of H
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(taddr + c * 32, v);
                     tmem_ld_wait();
@@ -506,6 +584,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             else mbar_arrive_cluster(leader_tempty + 8 * acc);
             acc ^= 1u;
             if (acc == 0) aphase ^= 1u;
+            if (PHASE == 3 && pt.ph == 1) {
+                // Publish this CTA's up_logits rows of the tile to the phase-2
+                // tiles of the unit, which read them with TMA: every storing
+                // thread orders its stores before later async-proxy reads, the
+                // four epilogue warps meet, then one thread releases a count.
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_THREADS) : "memory");
+                if (warp == 2 && lane == 0 && ti.store) {
+                    __threadfence();
+                    atomicAdd(p.ready + pt.t / pp.n_tiles, 1);
+                }
+            }
         }
     }
 
@@ -607,7 +697,11 @@ int device_sm_count() {
     return n;
 }
 
-cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream) {
+int64_t single_launch_workspace_bytes(int64_t num_blocks_m) {
+    return ((4 * num_blocks_m + 255) / 256) * 256;
+}
+
+cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream, void* ready_ws) {
     if (!encode_fn()) return cudaErrorNotSupported;
     CUtensorMap map_x, map_x16, map_gate, map_up, map_u, map_u16, map_down;
     const uint64_t rows = static_cast<uint64_t>(a.rows_total);
@@ -619,35 +713,37 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         !make_map_3d(&map_down, a.down_w, E, H, I, 128))
         return cudaErrorInvalidValue;
 
-    GemmParams p1{};
-    p1.sizes = a.sizes;
-    p1.offsets = a.offsets;
-    p1.padded = a.padded;
-    p1.gidx = a.gidx;
-    p1.rw = a.rw;
-    p1.status = a.status;
-    p1.rows_total = a.rows_total;
-    p1.valid_total = a.valid_total;
-    p1.num_blocks_m = static_cast<int32_t>(a.num_blocks_m);
-    p1.n_experts = a.n_experts;
-    GemmParams p2 = p1;
-    p1.dst = a.up_logits;
-    p1.k_blocks = a.hidden / (BK * KSUB);
-    p1.n_tiles = a.intermediate / 128;
-    p1.n_extent = a.intermediate;
-    p2.dst = a.out;
-    p2.k_blocks = a.intermediate / (BK * KSUB);
-    p2.n_tiles = (a.hidden + BN - 1) / BN;
-    p2.n_extent = a.hidden;
-    p2.tables_before_wait = (flags & MOE_RUN_PHASE1) ? 1 : 0;
+    GemmParams p{};
+    p.sizes = a.sizes;
+    p.offsets = a.offsets;
+    p.padded = a.padded;
+    p.gidx = a.gidx;
+    p.rw = a.rw;
+    p.status = a.status;
+    p.rows_total = a.rows_total;
+    p.valid_total = a.valid_total;
+    p.num_blocks_m = static_cast<int32_t>(a.num_blocks_m);
+    p.n_experts = a.n_experts;
+    p.ph[0].dst = a.up_logits;
+    p.ph[0].k_blocks = a.hidden / (BK * KSUB);
+    p.ph[0].n_tiles = a.intermediate / 128;
+    p.ph[0].n_extent = a.intermediate;
+    p.ph[1].dst = a.out;
+    p.ph[1].k_blocks = a.intermediate / (BK * KSUB);
+    p.ph[1].n_tiles = (a.hidden + BN - 1) / BN;
+    p.ph[1].n_extent = a.hidden;
+    p.tables_before_wait = (flags & MOE_RUN_PHASE1) ? 1 : 0;
+    p.ready = static_cast<int32_t*>(ready_ws);
 
     const size_t smem = smem_bytes_for(a.num_blocks_m);
     cudaError_t err = cudaSuccess;
-    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem))) != cudaSuccess)
-        return err;
-    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem))) != cudaSuccess)
+    const int smem_i = static_cast<int>(smem);
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_i)) !=
+            cudaSuccess ||
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_i)) !=
+            cudaSuccess ||
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_i)) !=
+            cudaSuccess)
         return err;
 
     cudaLaunchAttribute attr[2];
@@ -663,12 +759,26 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
+    const bool both = (flags & (MOE_RUN_PHASE1 | MOE_RUN_PHASE2)) == (MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
+    if (ready_ws != nullptr && both) {
+        // both phases in one persistent launch; the per-unit counters start at zero
+        err = cudaMemsetAsync(ready_ws, 0, static_cast<size_t>(single_launch_workspace_bytes(a.num_blocks_m)),
+                              stream);
+        if (err != cudaSuccess) return err;
+        const int nc = max_clusters<3>(smem);
+        if (nc <= 0) return cudaErrorNoDevice;
+        cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<3>, map_x, map_x16, map_gate, map_up, map_u, map_u16,
+                                  map_down, p);
+    }
     if (flags & MOE_RUN_PHASE1) {
         const int nc = max_clusters<1>(smem);
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = 2;   // cluster + programmatic dependent launch
-        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x16, map_gate, map_up, p1);
+        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x16, map_gate, map_up, map_x, map_x16,
+                                 map_gate, p);
         if (err != cudaSuccess) return err;
     }
     if (flags & MOE_RUN_PHASE2) {
@@ -679,7 +789,8 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = (flags & MOE_NO_PDL) ? 1 : 2;
-        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_u16, map_down, map_down, p2);
+        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_u16, map_down, map_down, map_u, map_u16,
+                                 map_down, p);
     }
     return err;
 }

@@ -138,14 +138,17 @@ moe_status_t moe_router_topk(const uint16_t* x_tokens, int64_t n_tokens, int32_t
                                         topk_weights, status_dev, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,
-                                  int32_t hidden, const uint16_t* gate_w, const uint16_t* up_w,
-                                  const uint16_t* down_w, int32_t n_experts, int32_t intermediate,
-                                  const float* routed_expert_weights, int64_t total_valid_tokens,
-                                  const int32_t* group_sizes, const int32_t* group_offsets,
-                                  const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx,
-                                  int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out,
-                                  int32_t* status_dev, void* stream, uint32_t flags) {
+}  // extern "C"
+
+namespace {
+
+moe_status_t forward_impl(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens, int32_t hidden,
+                          const uint16_t* gate_w, const uint16_t* up_w, const uint16_t* down_w, int32_t n_experts,
+                          int32_t intermediate, const float* routed_expert_weights, int64_t total_valid_tokens,
+                          const int32_t* group_sizes, const int32_t* group_offsets,
+                          const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx,
+                          int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out, int32_t* status_dev,
+                          void* stream, uint32_t flags, void* ready_ws) {
     const uint32_t phases = flags & (MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
     if (phases == 0 || (flags & ~(MOE_RUN_PHASE1 | MOE_RUN_PHASE2 | MOE_NO_PDL)) != 0)
         return MOE_ERR_SHAPE;
@@ -184,7 +187,46 @@ moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t
     a.up_logits = up_logits;
     a.out = out;
     a.status = status_dev;
-    return from_cuda(moe::launch_fused_forward(a, flags, static_cast<cudaStream_t>(stream)));
+    return from_cuda(moe::launch_fused_forward(a, flags, static_cast<cudaStream_t>(stream), ready_ws));
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_fused_forward_ex(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,
+                                  int32_t hidden, const uint16_t* gate_w, const uint16_t* up_w,
+                                  const uint16_t* down_w, int32_t n_experts, int32_t intermediate,
+                                  const float* routed_expert_weights, int64_t total_valid_tokens,
+                                  const int32_t* group_sizes, const int32_t* group_offsets,
+                                  const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx,
+                                  int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out,
+                                  int32_t* status_dev, void* stream, uint32_t flags) {
+    return forward_impl(stacked_expert_tokens, total_padded_tokens, hidden, gate_w, up_w, down_w, n_experts,
+                        intermediate, routed_expert_weights, total_valid_tokens, group_sizes, group_offsets,
+                        group_padded_offsets, group_idx_for_bx, num_blocks_m, up_logits, out, status_dev, stream,
+                        flags, nullptr);
+}
+
+int64_t moe_single_launch_workspace_bytes(int64_t num_blocks_m) {
+    if (num_blocks_m < 0) return -1;
+    return moe::single_launch_workspace_bytes(num_blocks_m);
+}
+
+moe_status_t moe_fused_forward_single_launch(
+    const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens, int32_t hidden, const uint16_t* gate_w,
+    const uint16_t* up_w, const uint16_t* down_w, int32_t n_experts, int32_t intermediate,
+    const float* routed_expert_weights, int64_t total_valid_tokens, const int32_t* group_sizes,
+    const int32_t* group_offsets, const int32_t* group_padded_offsets, const int32_t* group_idx_for_bx,
+    int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out, void* workspace, size_t workspace_bytes,
+    int32_t* status_dev, void* stream) {
+    if (num_blocks_m < 0) return MOE_ERR_SHAPE;
+    if (!workspace || static_cast<int64_t>(workspace_bytes) < moe::single_launch_workspace_bytes(num_blocks_m))
+        return MOE_ERR_WORKSPACE;
+    return forward_impl(stacked_expert_tokens, total_padded_tokens, hidden, gate_w, up_w, down_w, n_experts,
+                        intermediate, routed_expert_weights, total_valid_tokens, group_sizes, group_offsets,
+                        group_padded_offsets, group_idx_for_bx, num_blocks_m, up_logits, out, status_dev, stream,
+                        MOE_RUN_PHASE1 | MOE_RUN_PHASE2, workspace);
 }
 
 moe_status_t moe_fused_forward(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens,

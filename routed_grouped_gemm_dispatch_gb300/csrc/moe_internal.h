@@ -35,7 +35,11 @@ cudaError_t launch_build_dispatch(const int32_t* topk_ids, int64_t pairs, int32_
 
 // Enqueue phase 1 and/or phase 2 (MOE_RUN_* flags).  Arguments already validated.  Returns
 // cudaErrorNotSupported when the driver entry point for tensor maps is missing.
-cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream);
+// With `ready_ws` (zeroed here, single_launch_workspace_bytes() bytes) and both
+// phases requested, both phases run in one persistent launch.
+cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream,
+                                 void* ready_ws = nullptr);
+int64_t single_launch_workspace_bytes(int64_t num_blocks_m);
 
 // Pack: pair ranks, padded rows, compact routed weights, activation rows.
 int64_t pack_workspace_bytes(int64_t pairs, int32_t n_experts);

@@ -221,3 +221,66 @@ def test_dsv3_full_size_sampled_rows():
     valid_mask[side_g.pair_rows.reshape(-1).long()] = True
     pad_rows = out.view(torch.int16)[~valid_mask]
     assert bool((pad_rows == SENTINEL).all())
+
+
+# --------------------------------------------------------------------------
+# both phases in one persistent launch
+# --------------------------------------------------------------------------
+
+def _run_single_launch(side, intermediate, status=None):
+    from gpu_side import sentinel
+    ul = sentinel(side.rows_total, intermediate)
+    out = sentinel(side.rows_total, side.x_packed.shape[1])
+    t = side.tables
+    ws = torch.empty(moe.single_launch_workspace_bytes(t["group_idx_for_bx"].numel()), dtype=torch.uint8,
+                     device="cuda")
+    ws.fill_(0x5A)      # the call must zero its own counters
+    moe.fused_forward(side.x_packed, side.gate, side.up, side.down, side.rw, t["group_sizes"],
+                      t["group_offsets"], t["group_padded_offsets"], t["group_idx_for_bx"], ul, out,
+                      status=status, single_launch_workspace=ws)
+    return ul, out
+
+
+@pytest.mark.parametrize("shape", [
+    (300, 2, 3, 256, 384, "uniform"),
+    (500, 4, 40, 384, 256, "uniform"),
+    (32, 8, 128, 256, 256, "zipf"),
+    (700, 1, 2, 512, 640, "zipf"),
+])
+def test_single_launch_matches_two_launches_bit_for_bit(shape):
+    """Each tile is computed identically (same k order, same epilogue), so
+    the one-launch forward must reproduce the two-launch forward exactly —
+    including untouched padding rows — and stay within the oracle tolerance."""
+    T, k, E, H, I, routing = shape
+    w = small_workload(tokens=T, top_k=k, experts=E, hidden=H, intermediate=I,
+                       routing=routing, zipf_s=1.2 if routing == "zipf" else 0.0)
+    raw = raw_inputs(w, seed=6)
+    side = gpu_prepare(raw)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ul2, out2 = run_forward(side, I)
+    ul1, out1 = _run_single_launch(side, I, status=status)
+    ul1b, out1b = _run_single_launch(side, I, status=status)     # twice: counters re-zeroed per call
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for a, b in ((ul1, ul2), (out1, out2), (ul1b, ul2), (out1b, out2)):
+        assert np.array_equal(bits(a), bits(b))
+    side_o = oracle_prepare(raw)
+    up_o = np.full((side_o.rows_total, I), SENTINEL, np.uint16)
+    out_o = np.full((side_o.rows_total, H), SENTINEL, np.uint16)
+    oracle.fused_forward(side_o.x_packed, raw.gate, raw.up, raw.down, side_o.rw, side_o.tables, up_o, out_o)
+    v = _valid_mask(side_o.pair_rows, side_o.rows_total)
+    assert within_tol(bits(out1)[v], out_o[v], ATOL, RTOL).all()
+
+
+@pytest.mark.parametrize("name", ["dsv2_lite", "decode_skewed"])
+def test_single_launch_full_size_matches_two_launches(name):
+    w = workloads.WORKLOADS[name]
+    raw = raw_inputs(w, seed=0)
+    side = gpu_prepare(raw)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ul2, out2 = run_forward(side, w.intermediate)
+    ul1, out1 = _run_single_launch(side, w.intermediate, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(bits(out1), bits(out2))
+    assert np.array_equal(bits(ul1), bits(ul2))
