@@ -196,6 +196,11 @@ moe_status_t moe_router_topk(const uint16_t* x_tokens, int64_t n_tokens, int32_t
 #define MOE_RUN_PHASE1   0x1u  /* gate+up GEMM and SiLU·up epilogue into up_logits   */
 #define MOE_RUN_PHASE2   0x2u  /* down GEMM and routed-weight epilogue into out       */
 #define MOE_NO_PDL       0x4u  /* launch phase 2 without programmatic dependent launch */
+/* Test of the failure path: phase 1's MMA issuer skips its first "accumulator
+ * ready" signal, so an epilogue wait runs out after its bound (2 s); the
+ * kernel then stops, frees its resources and reports MOE_DEV_TIMEOUT in
+ * status_dev.  The outputs of such a call are not valid. */
+#define MOE_TEST_DROP_SIGNAL 0x100u
 
 /* moe_fused_forward with a choice of phases: `flags` is a combination of
  * MOE_RUN_PHASE1 / MOE_RUN_PHASE2 (at least one) and optionally MOE_NO_PDL.

@@ -37,6 +37,7 @@ MOE_DEV_TIMEOUT = 0x4
 MOE_RUN_PHASE1 = 0x1
 MOE_RUN_PHASE2 = 0x2
 MOE_NO_PDL = 0x4
+MOE_TEST_DROP_SIGNAL = 0x100
 
 _lock = threading.Lock()
 _lib = None

@@ -109,6 +109,7 @@ struct GemmParams {
                                  // waiting for phase 1 (phase 1 lets it start only after its own wait)
     int32_t* ready;           // both phases in one launch: per unit, finished phase-1 tile stores
                               // (zero at launch)
+    int32_t drop_first_signal;   // failure-path test: skip the first "accumulator ready" commit
 };
 
 // Rows of block bx that belong to its expert ("Fused MoE GEMM 提交说明",
@@ -504,7 +505,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit_pair_mc(bar_tfull + 8 * acc, CLUSTER_MASK);
+                if (!(p.drop_first_signal && t == cluster_id)) tc_commit_pair_mc(bar_tfull + 8 * acc, CLUSTER_MASK);
                 acc ^= 1u;
                 if (acc == 0) aphase ^= 1u;
             }
@@ -734,6 +735,7 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     p.ph[1].n_extent = a.hidden;
     p.tables_before_wait = (flags & MOE_RUN_PHASE1) ? 1 : 0;
     p.ready = static_cast<int32_t*>(ready_ws);
+    p.drop_first_signal = (flags & MOE_TEST_DROP_SIGNAL) ? 1 : 0;
 
     const size_t smem = smem_bytes_for(a.num_blocks_m);
     cudaError_t err = cudaSuccess;
@@ -780,6 +782,7 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x16, map_gate, map_up, map_x, map_x16,
                                  map_gate, p);
         if (err != cudaSuccess) return err;
+        p.drop_first_signal = 0;
     }
     if (flags & MOE_RUN_PHASE2) {
         // Phase 2 may start its prologue (tables, TMEM, barriers) while phase 1

@@ -150,7 +150,7 @@ moe_status_t forward_impl(const uint16_t* stacked_expert_tokens, int64_t total_p
                           int64_t num_blocks_m, uint16_t* up_logits, uint16_t* out, int32_t* status_dev,
                           void* stream, uint32_t flags, void* ready_ws) {
     const uint32_t phases = flags & (MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
-    if (phases == 0 || (flags & ~(MOE_RUN_PHASE1 | MOE_RUN_PHASE2 | MOE_NO_PDL)) != 0)
+    if (phases == 0 || (flags & ~(MOE_RUN_PHASE1 | MOE_RUN_PHASE2 | MOE_NO_PDL | MOE_TEST_DROP_SIGNAL)) != 0)
         return MOE_ERR_SHAPE;
     if (!stacked_expert_tokens || !gate_w || !up_w || !down_w ||
         (total_valid_tokens > 0 && !routed_expert_weights) || !group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx || !up_logits ||
