@@ -23,7 +23,7 @@
 //    rows) and the pair shares it.  Per SM this halves the weight bytes that
 //    TMA writes into and the tensor core reads out of shared memory, which is
 //    what limits a one-SM 128 x 256 tile.  A single block runs the same tile
-//    with its rows repeated in the odd CTA, whose results are not stored.
+//    with zero rows in the odd CTA, whose results are not stored.
 //  * Inside a CTA: warp 0 issues TMA loads (128-byte swizzled tiles, 6-stage
 //    ring; both CTAs' copies complete on the even CTA's "full" barrier), warp 1
 //    owns TMEM (allocated for the pair) and, in the even CTA only, issues the
@@ -399,10 +399,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 }
                 const int32_t size_next = __ldg(p.sizes + e_next), pad_next = __ldg(p.padded + e_next);
                 const int32_t e_next2 = expert_of(t + 2 * n_clusters);
-                // Rows of A to load: none for the odd CTA of a single block
-                // (its rows of D are discarded, stale shared memory serves);
-                // 16-row boxes for a block with at most SMALL_ROWS valid rows
-                // (decode-like blocks); otherwise the full 128-row box, which
+                // Rows of A to load.  The odd CTA of a single block loads a box
+                // that lies wholly past the tensor's last row: it reads no
+                // memory and lands as zeros, so the discarded half of the tile
+                // multiplies zeros (on a power-capped GPU this measured ~2%
+                // faster than multiplying whatever the stage last held).  A
+                // block with at most SMALL_ROWS valid rows (decode-like) loads
+                // 16-row boxes; every other block the full 128-row box, which
                 // moves faster than many small boxes.  Rows not loaded only
                 // feed discarded rows of D.  (Only the even CTA, which sets the
                 // expected byte count, needs the odd CTA's count.)
@@ -414,11 +417,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 auto a_bytes = [&](int32_t boxes) -> uint32_t {
                     return boxes == 0 ? A_BOX_BYTES : boxes * (A_BOX_BYTES / 8);
                 };
-                const bool load_a = ti.store;
-                const int32_t boxes_own = load_a ? a_boxes(ti.bx) : 0;
-                const uint32_t bytes_peer = (leader && ti.pair) ? a_bytes(a_boxes(ti.bx0 + 1)) : 0;
-                const uint32_t stage_tx =
-                    KSUB * ((load_a ? a_bytes(boxes_own) : 0) + bytes_peer + 2 * B_BOX_BYTES);
+                const int32_t a_row = ti.store ? ti.bx * BM : static_cast<int32_t>(p.rows_total);
+                const int32_t boxes_own = ti.store ? a_boxes(ti.bx) : 0;
+                const uint32_t bytes_peer =
+                    !leader ? 0u : ti.pair ? a_bytes(a_boxes(ti.bx0 + 1)) : static_cast<uint32_t>(A_BOX_BYTES);
+                const uint32_t stage_tx = KSUB * (a_bytes(boxes_own) + bytes_peer + 2 * B_BOX_BYTES);
                 for (int32_t kb = 0; kb < pp.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -431,9 +434,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {
                         const int32_t k0 = (kb * KSUB + ks) * BK;
-                        if (load_a && boxes_own == 0) {
-                            tma_load_2d_pair(sa + ks * A_BOX_BYTES, a_map, fb, k0, ti.bx * BM, pol_a);
-                        } else if (load_a) {
+                        if (boxes_own == 0) {
+                            tma_load_2d_pair(sa + ks * A_BOX_BYTES, a_map, fb, k0, a_row, pol_a);
+                        } else {
                             for (int32_t b = 0; b < boxes_own; ++b)
                                 tma_load_2d_pair(sa + ks * A_BOX_BYTES + b * (A_BOX_BYTES / 8), a16_map, fb, k0,
                                                  ti.bx * BM + b * 16, pol_a);
