@@ -48,24 +48,39 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
     __syncthreads();
 
-    // histogram of the flattened expert ids
+    // histogram of the flattened expert ids: 16-byte loads, eight per thread
+    // in flight before their atomics, so a few memory round trips cover the
+    // whole input; a scalar loop takes the unaligned case and the tail
     bool bad = false;
-    int64_t f = tid;
-    for (; f + 3 * DISPATCH_THREADS < pairs; f += 4 * DISPATCH_THREADS) {
-        int32_t v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldg(topk_ids + f + u * DISPATCH_THREADS);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (static_cast<uint32_t>(v[u]) < static_cast<uint32_t>(n_experts)) atomicAdd(&cnt[v[u]], 1);
-            else bad = true;
-        }
-    }
-    for (; f < pairs; f += DISPATCH_THREADS) {
-        const int32_t v = __ldg(topk_ids + f);
+    auto count = [&](int32_t v) {
         if (static_cast<uint32_t>(v) < static_cast<uint32_t>(n_experts)) atomicAdd(&cnt[v], 1);
         else bad = true;
+    };
+    int64_t done = 0;
+    if ((reinterpret_cast<uintptr_t>(topk_ids) & 15) == 0) {
+        constexpr int U = 8;
+        const int64_t n4 = pairs / 4;
+        const int4* ids4 = reinterpret_cast<const int4*>(topk_ids);
+        for (int64_t base = 0; base < n4; base += U * DISPATCH_THREADS) {
+            int4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + u * DISPATCH_THREADS + tid;
+                if (i < n4) v[u] = __ldg(ids4 + i);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (base + u * DISPATCH_THREADS + tid < n4) {
+                    count(v[u].x);
+                    count(v[u].y);
+                    count(v[u].z);
+                    count(v[u].w);
+                }
+            }
+        }
+        done = 4 * n4;
     }
+    for (int64_t f = done + tid; f < pairs; f += DISPATCH_THREADS) count(__ldg(topk_ids + f));
     if (bad && status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
 
