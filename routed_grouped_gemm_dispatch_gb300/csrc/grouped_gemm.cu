@@ -24,8 +24,9 @@
 //    TMA writes into and the tensor core reads out of shared memory, which is
 //    what limits a one-SM 128 x 256 tile.  A single block runs the same tile
 //    with zero rows in the odd CTA, whose results are not stored.
-//  * Inside a CTA: warp 0 issues TMA loads (128-byte swizzled tiles, 6-stage
-//    ring; both CTAs' copies complete on the even CTA's "full" barrier), warp 1
+//  * Inside a CTA: warp 0 issues TMA loads (128-byte swizzled tiles; a ring of
+//    three 64 KB stages, each two adjacent 64-wide K boxes of A and of B; both
+//    CTAs' copies complete on the even CTA's "full" barrier), warp 1
 //    owns TMEM (allocated for the pair) and, in the even CTA only, issues the
 //    MMAs (K = 16 each, fp32 accumulators in TMEM, double buffered so the
 //    epilogue of one tile overlaps the MMAs of the next), warps 2-5 run the
@@ -51,7 +52,7 @@ namespace {
 
 constexpr int BM = 128;                       // rows per block (block_token)
 constexpr int BK = 64;                        // K per box: one 128-byte swizzle row
-constexpr int KSUB = 1;                       // boxes (adjacent 64-wide K chunks) per stage
+constexpr int KSUB = 2;                       // boxes (adjacent 64-wide K chunks) per stage
 constexpr int BN = 256;                       // N per MMA
 constexpr int STAGES = 6 / KSUB;
 constexpr int A_BOX_BYTES = BM * BK * 2;      // 16 KB: this CTA's 128 rows of A, one box
