@@ -26,6 +26,10 @@ import os
 import threading
 
 BLOCK_TOKEN = 128
+MAX_EXPERTS = 1024          # MOE_MAX_EXPERTS
+MAX_BLOCKS = 16384          # MOE_MAX_BLOCKS
+ROUTER_MAX_EXPERTS = 256    # MOE_ROUTER_MAX_EXPERTS
+ROUTER_MAX_TOPK = 16        # MOE_ROUTER_MAX_TOPK
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")

@@ -95,3 +95,15 @@ def test_dispatch_host_validation(L):
     assert call(k=0) == -2
     assert call(s=None) == -1
     assert call(ids=None) == -1
+
+
+def test_binding_limits_match_header():
+    import re
+    import routed_grouped_gemm_dispatch_gb300 as moe
+    text = open(os.path.join(ROOT, "include", "moe_gb300.h")).read()
+    defs = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (MOE_\w+)\s+(\d+)\b", text)}
+    assert defs["MOE_BLOCK_TOKEN"] == moe.BLOCK_TOKEN
+    assert defs["MOE_MAX_EXPERTS"] == moe.MAX_EXPERTS
+    assert defs["MOE_MAX_BLOCKS"] == moe.MAX_BLOCKS
+    assert defs["MOE_ROUTER_MAX_EXPERTS"] == moe.ROUTER_MAX_EXPERTS
+    assert defs["MOE_ROUTER_MAX_TOPK"] == moe.ROUTER_MAX_TOPK

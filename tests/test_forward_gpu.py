@@ -223,6 +223,38 @@ def test_dsv3_full_size_sampled_rows():
     assert bool((pad_rows == SENTINEL).all())
 
 
+def test_forward_at_block_and_expert_limits():
+    """num_blocks_m = MOE_MAX_BLOCKS and n_experts = MOE_MAX_EXPERTS (H = I = 128,
+    top-8 uniform routing over 245,760 tokens): the largest active-block list
+    and unit list the kernels keep in shared memory.  Sampled valid rows against
+    the oracle; every padding row untouched (checked on the device)."""
+    E, k = moe.MAX_EXPERTS, 8
+    T = (moe.MAX_BLOCKS - E) * BT // k
+    w = small_workload(tokens=T, top_k=k, experts=E, hidden=128, intermediate=128)
+    raw = raw_inputs(w, seed=5)
+    side_o = oracle_prepare(raw)
+    assert side_o.tables["num_blocks_m"] == moe.MAX_BLOCKS
+    side_g = gpu_prepare(raw)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ul, out = run_forward(side_g, w.intermediate, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = _sample_rows(side_o.pair_rows, side_o.tables, np.random.default_rng(2), n_random=64)
+    up_r, out_r, valid = oracle.forward_rows(side_o.x_packed, raw.gate, raw.up, raw.down,
+                                             side_o.rw, side_o.tables, rows)
+    assert valid.all()
+    idx = torch.from_numpy(rows).cuda()
+    up_g = ul.view(torch.int16)[idx].cpu().numpy().view(np.uint16)
+    out_g = out.view(torch.int16)[idx].cpu().numpy().view(np.uint16)
+    assert within_tol(up_g, up_r, ATOL, RTOL).all()
+    assert within_tol(out_g, out_r, ATOL, RTOL).all()
+    valid_mask = torch.zeros(side_o.rows_total, dtype=torch.bool, device="cuda")
+    valid_mask[side_g.pair_rows.reshape(-1).long()] = True
+    assert bool((out.view(torch.int16)[~valid_mask] == SENTINEL).all())
+    assert bool((ul.view(torch.int16)[~valid_mask] == SENTINEL).all())
+    assert bool((out.view(torch.int16)[valid_mask] != SENTINEL).all())
+
+
 # --------------------------------------------------------------------------
 # both phases in one persistent launch
 # --------------------------------------------------------------------------
