@@ -287,6 +287,22 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(ms, dist, device):
+    """The job's step time: the slowest rank's (one all-reduce; identity on one rank)."""
+    if dist is None:
+        return ms
+    import torch
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(world, flops_per_rank, ms):
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload
+    (weak scaling), so the job does world x the per-rank FLOPs per step."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def config_of(w, l2):
     return {"workload": w.name, "tokens": w.tokens, "top_k": w.top_k, "experts": w.experts,
             "hidden": w.hidden, "intermediate": w.intermediate, "pairs": w.pairs,
@@ -374,14 +390,10 @@ def main():
     torch.cuda.synchronize(dev)
     sampler.mark_end()
     barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, dev)
     sampler.stop()
     flops = w.flops()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_value(world, flops, ms)
 
     # ---- per-phase durations (same stream, CUDA events) -------------------
     n_ph = max(5, min(args.steps, 50))
@@ -482,7 +494,7 @@ def main():
         comp.wait_stream(s_out)
         b.record(comp)
         torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, dist, dev)
         for _ in range(3):
             e2e_step_serial()
         torch.cuda.synchronize(dev)
@@ -491,15 +503,15 @@ def main():
             e2e_step_serial()
         b.record(comp)
         torch.cuda.synchronize(dev)
-        serial_ms = a.elapsed_time(b) / n_e2e
+        serial_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, dist, dev)
         y_ok = bool(torch.equal(h_y[0].to(dev), d_y[0]))
         h2d = h_ids.numel() * 4 + h_x.numel() * 2 + h_tw.numel() * 4
         d2h = h_y[0].numel() * 2
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e = {"value": job_value(world, flops, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": n_e2e, "gpu_launches_per_step": 7, "pipelined": True,
                "serial_ms_per_step": serial_ms,
-               "serial_value": world * flops / (serial_ms * 1e-3) / 1e12,
+               "serial_value": job_value(world, flops, serial_ms),
                "host_copy_matches_device": y_ok,
                "path": "pinned host tokens [T,H] + topk_ids + topk weights -> H2D -> moe_build_dispatch -> "
                        "moe_pack_routed -> moe_fused_forward -> moe_combine_routed -> D2H token outputs [T,H]; "
@@ -554,12 +566,12 @@ def main():
             return a.elapsed_time(b) / n
 
         n_sc = max(5, min(args.steps, 100))
-        cached_ms = time_fn(lambda: layer(x_l), n_sc)
-        host_ms = time_fn(layer_host, n_sc)
+        cached_ms = max_over_ranks(time_fn(lambda: layer(x_l), n_sc), dist, dev)
+        host_ms = max_over_ranks(time_fn(layer_host, n_sc), dist, dev)
         router_flops = 2.0 * w.tokens * w.hidden * w.experts
         scopes = {"routed_kernel_only_ms": ms, "cached_e2e_ms": cached_ms, "e2e_host_ms": host_ms,
-                  "cached_e2e_tflops": world * (flops + router_flops) / (cached_ms * 1e-3) / 1e12,
-                  "e2e_host_tflops": world * (flops + router_flops) / (host_ms * 1e-3) / 1e12,
+                  "cached_e2e_tflops": job_value(world, flops + router_flops, cached_ms),
+                  "e2e_host_tflops": job_value(world, flops + router_flops, host_ms),
                   "flops_note": "expert FLOPs 6*P*H*I plus router 2*T*H*E; routing from a random "
                                 "router (near-uniform), not the workload's own routing",
                   "launches_per_layer": 8}
