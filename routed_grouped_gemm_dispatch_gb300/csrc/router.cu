@@ -6,9 +6,10 @@
 // N = n_experts rounded up to 16 (at most 256), so a token's whole logit row
 // sits in one TMEM lane.  Warp 0 streams x and W_g with TMA (4 stages of
 // 64-wide K), warp 1 owns TMEM and issues the MMAs, warps 2-5 each take 32
-// tokens: an online softmax (running max and rescaled sum) and a register
-// top-k over the row, ties to the lower expert index, written in descending
-// order.  The top-k is decided on the logits (softmax preserves their order).
+// tokens: a register top-k over the row (ties to the lower expert index,
+// written in descending order), then the softmax denominator over all experts
+// against the row maximum.  The top-k is decided on the logits (softmax
+// preserves their order).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -153,44 +154,64 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         if (mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS)) {
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            float m = -INFINITY, s = 0.0f;
+            // Two passes over the row in TMEM, everything in registers (every
+            // loop over a chunk or the list is unrolled with compile-time
+            // indices).  Pass 1 keeps the R_MAX_TOPK largest logits in a
+            // descending list: a new value goes in after any equal one (the
+            // lower expert index stays first), and every slot is updated from
+            // the old list at once instead of by a serial walk.  Pass 2 sums
+            // exp(l - max) with independent partial sums.
             float best_v[R_MAX_TOPK];
             int32_t best_i[R_MAX_TOPK];
-            for (int j = 0; j < R_MAX_TOPK; ++j) {
-                best_v[j] = -INFINITY;
-                best_i[j] = -1;
+#pragma unroll
+            for (int q = 0; q < R_MAX_TOPK; ++q) {
+                best_v[q] = -INFINITY;
+                best_i[q] = -1;
             }
+            // (8 columns per TMEM load keeps the unrolled insertion code small
+            // enough for the instruction cache)
+            for (int32_t c0 = 0; c0 < p.n_pad; c0 += 8) {
+                uint32_t v[8];
+                tmem_ld_32x32b_x8(taddr + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int32_t e = c0 + j;
+                    const float l = __uint_as_float(v[j]);
+                    if (e < p.n_experts && (best_i[R_MAX_TOPK - 1] < 0 || l > best_v[R_MAX_TOPK - 1])) {
+                        bool gt[R_MAX_TOPK];
+#pragma unroll
+                        for (int q = 0; q < R_MAX_TOPK; ++q) gt[q] = best_i[q] < 0 || l > best_v[q];
+#pragma unroll
+                        for (int q = R_MAX_TOPK - 1; q > 0; --q) {
+                            best_v[q] = gt[q - 1] ? best_v[q - 1] : (gt[q] ? l : best_v[q]);
+                            best_i[q] = gt[q - 1] ? best_i[q - 1] : (gt[q] ? e : best_i[q]);
+                        }
+                        if (gt[0]) {
+                            best_v[0] = l;
+                            best_i[0] = e;
+                        }
+                    }
+                }
+            }
+            const float mx = best_v[0];
+            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             for (int32_t c0 = 0; c0 < p.n_pad; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
-                for (int j = 0; j < 32; ++j) {
-                    const int32_t e = c0 + j;
-                    if (e >= p.n_experts) break;
-                    const float l = __uint_as_float(v[j]);
-                    if (l > m) {
-                        s = s * expf(m - l) + 1.0f;
-                        m = l;
-                    } else {
-                        s += expf(l - m);
-                    }
-                    // insert after any equal value: equal logits keep the lower index first
-                    if (best_i[p.top_k - 1] < 0 || l > best_v[p.top_k - 1]) {
-                        int32_t pos = p.top_k - 1;
-                        while (pos > 0 && (best_i[pos - 1] < 0 || l > best_v[pos - 1])) {
-                            best_v[pos] = best_v[pos - 1];
-                            best_i[pos] = best_i[pos - 1];
-                            --pos;
-                        }
-                        best_v[pos] = l;
-                        best_i[pos] = e;
-                    }
-                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < p.n_experts) part[j & 3] += expf(__uint_as_float(v[j]) - mx);
             }
+            const float s = (part[0] + part[1]) + (part[2] + part[3]);
             if (t < p.n_tokens) {
-                for (int j = 0; j < p.top_k; ++j) {
-                    p.topk_ids[t * p.top_k + j] = best_i[j];
-                    p.topk_weights[t * p.top_k + j] = expf(best_v[j] - m) / s;
+#pragma unroll
+                for (int q = 0; q < R_MAX_TOPK; ++q) {
+                    if (q < p.top_k) {
+                        p.topk_ids[t * p.top_k + q] = best_i[q];
+                        p.topk_weights[t * p.top_k + q] = expf(best_v[q] - mx) / s;
+                    }
                 }
             }
         }
