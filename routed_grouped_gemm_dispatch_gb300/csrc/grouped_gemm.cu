@@ -70,6 +70,8 @@ constexpr int SMALL_ROWS = 32;                // blocks with at most this many r
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s per drain wait
 constexpr uint32_t IDESC = idesc_f16_f32acc(2 * BM, BN);   // M = 256 across the pair
+constexpr int64_t GROUP_A_BYTES = 32ll << 20;     // A rows a tile-order group keeps hot in L2
+constexpr int32_t UNITS_PER_EXPERT_MULT = 1;
 
 static_assert(MOE_MAX_BLOCKS <= 0x7FFF, "block indices must leave the pair bit free");
 
@@ -92,6 +94,7 @@ struct PhaseParams {
     int32_t k_blocks;         // K / (64 * KSUB)
     int32_t n_tiles;          // N slices per block
     int32_t n_extent;         // I (phase 1) or H (phase 2): columns of dst
+    int32_t group;            // largest group of the tile order the L2 budget allows (>= 1)
 };
 
 struct GemmParams {
@@ -140,9 +143,14 @@ __device__ __forceinline__ int32_t block_rows(const GemmParams& p, int32_t bx, i
     return static_cast<int32_t>(actual);
 }
 
-// One cluster tile as seen by the CTA of rank `rank`: unit t / n_tiles, slice
-// t % n_tiles.
+// One cluster tile as seen by the CTA of rank `rank`.  Tile order: the unit
+// list (expert-sorted) is cut into groups of `group` consecutive units, and
+// inside a group the tiles run slice by slice, each slice over all the
+// group's units.  Concurrent clusters then share each weight slice across an
+// expert's units while the group's A rows stay in L2; group = 1 is plain
+// unit-major order.
 struct Tile {
+    int32_t u;        // unit
     int32_t bx0;      // first block of the unit (the expert comes from it)
     int32_t bx;       // block whose rows this CTA holds
     int32_t n;        // N slice
@@ -151,10 +159,16 @@ struct Tile {
 };
 
 __device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, int32_t n_tiles,
-                                            uint32_t rank) {
-    const int32_t u = t / n_tiles;
+                                            int32_t nunits, int32_t group, uint32_t rank) {
+    const int32_t per_group = group * n_tiles;
+    const int32_t g = t / per_group;
+    const int32_t l = t - g * per_group;
+    const int32_t left = nunits - g * group;
+    const int32_t gsize = left < group ? left : group;
     Tile ti;
-    ti.n = t - u * n_tiles;
+    ti.n = l / gsize;
+    const int32_t u = g * group + (l - ti.n * gsize);
+    ti.u = u;
     ti.bx0 = units[u] & 0x7FFF;
     ti.pair = (units[u] & PAIR_BIT) != 0;
     ti.bx = ti.pair ? ti.bx0 + static_cast<int32_t>(rank) : ti.bx0;
@@ -346,6 +360,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     // stream the weights through L2 with evict-first; otherwise keep them for
     // the expert's other units.
     const bool weights_streamed = 4 * counts[1] <= 5 * counts[0];
+    // Tile-order group: about one expert's units (so a weight slice is shared
+    // by all of them at once), at most what the host's L2 budget allows.
+    const int32_t upe = counts[0] > 0 ? UNITS_PER_EXPERT_MULT * ((counts[1] + counts[0] - 1) / counts[0]) : 1;
+    const int32_t grp[2] = {p.ph[0].group < upe ? p.ph[0].group : upe,
+                            p.ph[1].group < upe ? p.ph[1].group : upe};
     // Both CTAs' barriers are initialised and their prologue scratch in the
     // stage area is dead before either CTA's copies or commits reach the other.
     cluster_sync_all();
@@ -373,7 +392,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             auto expert_of = [&](int32_t tt) -> int32_t {
                 if (tt >= total_tiles) return 0;
                 const PhaseTile pt = phase_of<PHASE>(tt, tiles1);
-                return __ldg(p.gidx + decode_tile(pt.t, units, p.ph[pt.ph - 1].n_tiles, rank).bx0);
+                const PhaseParams& q = p.ph[pt.ph - 1];
+                return __ldg(p.gidx + decode_tile(pt.t, units, q.n_tiles, counts[1], grp[pt.ph - 1], rank).bx0);
             };
             int32_t e_cur = expert_of(cluster_id);
             int32_t size_cur = __ldg(p.sizes + e_cur), pad_cur = __ldg(p.padded + e_cur);
@@ -381,7 +401,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             for (int32_t t = cluster_id; t < total_tiles && ok; t += n_clusters) {
                 const PhaseTile pt = phase_of<PHASE>(t, tiles1);
                 const PhaseParams& pp = p.ph[pt.ph - 1];
-                const Tile ti = decode_tile(pt.t, units, pp.n_tiles, rank);
+                const Tile ti = decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank);
                 const int32_t e = e_cur;
                 const CUtensorMap* a_map = pt.ph == 1 ? &map_x : &map_u;
                 const CUtensorMap* a16_map = pt.ph == 1 ? &map_x16 : &map_u16;
@@ -390,7 +410,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                     // phase-1 tile of the unit has stored them (both CTAs for a
                     // pair, the even CTA for a single), then order those generic
                     // stores before this thread's TMA (async proxy) reads
-                    const int32_t u = pt.t / pp.n_tiles;
+                    const int32_t u = ti.u;
                     const int32_t need = p.ph[0].n_tiles * (ti.pair ? 2 : 1);
                     if (!counter_wait_bounded(p.ready + u, need, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -528,7 +548,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int32_t t = cluster_id; t < total_tiles; t += n_clusters) {
             const PhaseTile pt = phase_of<PHASE>(t, tiles1);
             const PhaseParams& pp = p.ph[pt.ph - 1];
-            const Tile ti = decode_tile(pt.t, units, pp.n_tiles, rank);
+            const Tile ti = decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank);
             int32_t e = 0, tok = 0;
             const int32_t actual = ti.store ? block_rows(p, ti.bx, &e, &tok) : 0;
             if (!mbar_wait_bounded(bar_tfull + 8 * acc, aphase, abort_flag, WAIT_LIMIT_NS)) break;
@@ -598,7 +618,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_THREADS) : "memory");
                 if (warp == 2 && lane == 0 && ti.store) {
                     __threadfence();
-                    atomicAdd(p.ready + pt.t / pp.n_tiles, 1);
+                    atomicAdd(p.ready + ti.u, 1);
                 }
             }
         }
@@ -737,6 +757,15 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     p.ph[1].k_blocks = a.intermediate / (BK * KSUB);
     p.ph[1].n_tiles = (a.hidden + BN - 1) / BN;
     p.ph[1].n_extent = a.hidden;
+    // Group size of the tile order: as many units as keep their A rows
+    // (256 rows x K fp16 per unit) within GROUP_A_BYTES, 1 to 32.
+    auto group_for = [](int64_t k) {
+        const int64_t per_unit = 2 * BM * k * 2;
+        int64_t g = GROUP_A_BYTES / per_unit;
+        return static_cast<int32_t>(g < 1 ? 1 : (g > 32 ? 32 : g));
+    };
+    p.ph[0].group = group_for(a.hidden);
+    p.ph[1].group = group_for(a.intermediate);
     p.tables_before_wait = (flags & MOE_RUN_PHASE1) ? 1 : 0;
     p.ready = static_cast<int32_t*>(ready_ws);
     p.drop_first_signal = (flags & MOE_TEST_DROP_SIGNAL) ? 1 : 0;

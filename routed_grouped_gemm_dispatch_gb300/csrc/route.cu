@@ -10,12 +10,12 @@
 // Python loop and combine with a PyTorch scatter_reduce; here both are kernels.
 //
 // Pack runs in three launches:
-//   1. rank_chunks_kernel: for each chunk of PACK_CHUNK pairs, every pair's
+//   1. rank_chunks_kernel: for each chunk of PACK_CHUNK (1024) pairs, every pair's
 //      rank among the chunk's earlier pairs of the same expert (warp match_any
 //      inside a warp, shared-memory per-warp counts across warps) and the
 //      chunk's per-expert histogram (workspace);
-//   2. scan_chunks_kernel: per expert, exclusive prefix of the histograms over
-//      chunks (in place);
+//   2. scan_chunks_kernel: per expert (one warp each), exclusive prefix of the
+//      histograms over chunks (in place);
 //   3. place_pairs_kernel: row = padded[e] + chunk prefix + rank; writes the
 //      pair's padded row, its routed weight at the compact index, and copies
 //      the token's activation row (one warp per pair, 16-byte vectors).
@@ -33,7 +33,7 @@ namespace {
 
 constexpr int RANK_THREADS = 1024;
 constexpr int RANK_WARPS = RANK_THREADS / 32;
-constexpr int PACK_CHUNK = 4 * RANK_THREADS;       // pairs per chunk
+constexpr int PACK_CHUNK = RANK_THREADS;           // pairs per chunk (one pass per CTA)
 
 __global__ void __launch_bounds__(RANK_THREADS)
 rank_chunks_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32_t n_experts,
@@ -82,15 +82,25 @@ rank_chunks_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32_t 
     if (bad && status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
 }
 
+// One warp per expert: exclusive prefix of that expert's chunk histograms
+// (in place), 32 chunks per step with a warp-shuffle scan.
 __global__ void scan_chunks_kernel(int32_t* chunk_hist, int32_t n_chunks, int32_t n_experts) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int32_t e = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
     if (e >= n_experts) return;
-    int32_t acc = 0;
-    for (int32_t c = 0; c < n_chunks; ++c) {
+    int32_t carry = 0;
+    for (int32_t c0 = 0; c0 < n_chunks; c0 += 32) {
+        const int32_t c = c0 + lane;
         int32_t* p = chunk_hist + static_cast<int64_t>(c) * n_experts + e;
-        const int32_t v = *p;
-        *p = acc;
-        acc += v;
+        const int32_t v = c < n_chunks ? *p : 0;
+        int32_t incl = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += o;
+        }
+        if (c < n_chunks) *p = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
     }
 }
 
@@ -188,7 +198,7 @@ cudaError_t launch_pack(const int32_t* topk_ids, const float* topk_weights, int6
     if (err != cudaSuccess) return err;
     rank_chunks_kernel<<<chunks, RANK_THREADS, smem, stream>>>(topk_ids, pairs, n_experts, local_rank, hist,
                                                                status);
-    scan_chunks_kernel<<<(n_experts + 255) / 256, 256, 0, stream>>>(hist, chunks, n_experts);
+    scan_chunks_kernel<<<(n_experts + 7) / 8, 256, 0, stream>>>(hist, chunks, n_experts);
     const int64_t warps = pairs;
     const int64_t blocks = (warps * 32 + 255) / 256;
     place_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
