@@ -143,11 +143,17 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """Hash of the GEMM kernels' code (comments and layout stripped), so that
+    the DRAM traffic in profiles/ is only used for the kernel it was taken on."""
+    import re
     h = hashlib.sha256()
     for rel in ("routed_grouped_gemm_dispatch_gb300/csrc/grouped_gemm.cu",
                 "routed_grouped_gemm_dispatch_gb300/csrc/sm103_ptx.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -24,6 +24,9 @@
 //    TMA writes into and the tensor core reads out of shared memory, which is
 //    what limits a one-SM 128 x 256 tile.  A single block runs the same tile
 //    with zero rows in the odd CTA, whose results are not stored.
+//  * Tiles are ordered in groups of about one expert's units, slice by slice
+//    inside a group (see decode_tile), so concurrent clusters share each
+//    weight slice in L2 instead of re-reading it once per unit.
 //  * Inside a CTA: warp 0 issues TMA loads (128-byte swizzled tiles; a ring of
 //    three 64 KB stages, each two adjacent 64-wide K boxes of A and of B; both
 //    CTAs' copies complete on the even CTA's "full" barrier), warp 1
