@@ -59,6 +59,8 @@ typedef int32_t moe_status_t;
 #define MOE_DEV_BAD_EXPERT_ID 0x1  /* a topk id outside [0, n_experts)                 */
 #define MOE_DEV_BAD_TABLE     0x2  /* a table entry points outside its array           */
 #define MOE_DEV_TIMEOUT       0x4  /* a bounded pipeline wait ran out; tiles skipped    */
+#define MOE_DEV_DEBUG_CHECK   0x8  /* MOE_DEBUG builds only: a kernel's own check of an
+                                      index, coordinate or shared-memory canary failed */
 
 #define MOE_BLOCK_TOKEN  128
 #define MOE_MAX_EXPERTS  1024

@@ -32,12 +32,16 @@ ROUTER_MAX_EXPERTS = 256    # MOE_ROUTER_MAX_EXPERTS
 ROUTER_MAX_TOPK = 16        # MOE_ROUTER_MAX_TOPK
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
+# MOE_GB300_DEBUG=1 in the environment selects the MOE_DEBUG build (kernels
+# that also check their own indices and report MOE_DEV_DEBUG_CHECK).
+LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300_debug.so" if os.environ.get("MOE_GB300_DEBUG") == "1"
+                        else "libmoe_gb300.so")
 
 MOE_OK = 0
 MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_BAD_TABLE = 0x2
 MOE_DEV_TIMEOUT = 0x4
+MOE_DEV_DEBUG_CHECK = 0x8
 MOE_RUN_PHASE1 = 0x1
 MOE_RUN_PHASE2 = 0x2
 MOE_NO_PDL = 0x4
@@ -55,10 +59,11 @@ class MoeError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)} ({status})")
 
 
-def build(force: bool = False) -> str:
-    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+def build(force: bool = False, debug: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a); debug=True builds the
+    MOE_DEBUG variant."""
     from . import _build
-    return _build.build(force=force)
+    return _build.build(force=force, debug=debug)
 
 
 def lib():

@@ -2,7 +2,10 @@
 
 Each translation unit is compiled in parallel to an object file, then linked
 into ``_build/libmoe_gb300.so``.  Rebuilds only when a source is newer than
-the library.
+the library.  ``build(debug=True)`` makes ``_build/libmoe_gb300_debug.so`` with
+``-DMOE_DEBUG=1``: the kernels then also check their own indices, coordinates
+and shared-memory layout and report a failed check as MOE_DEV_DEBUG_CHECK in
+the status word (the stand-in for a sanitizer, which this pool does not run).
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
+LIB_DEBUG = os.path.join(BUILD, "libmoe_gb300_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,22 +44,26 @@ def _deps():
                                + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    target = LIB_DEBUG if debug else LIB
+    if not force and not needs_build(target):
+        return target
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if debug:
+        extra += ["-DMOE_DEBUG=1"]
+    tag = "dbg" if debug else "rel"
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + f".{os.getpid()}.o")
+        obj = os.path.join(BUILD, os.path.basename(src) + f".{tag}.{os.getpid()}.o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,17 +76,17 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = target + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart=static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, target)
     for o in objs:
         os.remove(o)
-    return LIB
+    return target
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, verbose_ptxas="-v" in sys.argv))
+    print(build(force=True, verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

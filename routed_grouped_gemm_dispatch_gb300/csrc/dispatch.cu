@@ -129,7 +129,13 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
             else hi = mid - 1;
         }
         gidx[bx] = lo;
+        // the found expert's padded range holds the block (or it is the last expert)
+        MOE_DCHECK(lo >= 0 && lo < n_experts && pad_s[lo] <= start &&
+                       (lo == n_experts - 1 || start < static_cast<int64_t>(pad_s[lo + 1])),
+                   status);
     }
+    // every padded range holds its rows plus at least one padding row, in whole blocks
+    MOE_DCHECK(e >= n_experts || (excl_p % block_token == 0 && step >= c + 1), status);
 }
 
 }  // namespace

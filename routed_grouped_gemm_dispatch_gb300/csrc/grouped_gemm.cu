@@ -90,7 +90,10 @@ constexpr int OFF_WSUM = OFF_COUNTS + 8;                       // NUM_THREADS/32
 constexpr int OFF_UNITS = ((OFF_WSUM + (NUM_THREADS / 32) * 4 + 15) / 16) * 16;
 
 __host__ __device__ inline size_t units_bytes(int64_t m) { return ((2 * static_cast<size_t>(m) + 15) / 16) * 16; }
-size_t smem_bytes_for(int64_t m) { return 1024 /* alignment slack */ + OFF_UNITS + units_bytes(m); }
+size_t smem_bytes_for(int64_t m) {
+    return 1024 /* alignment slack */ + OFF_UNITS + units_bytes(m) + (MOE_DEBUG ? 16 : 0);
+}
+constexpr uint32_t SMEM_CANARY = 0xC0FFEE11u;
 
 struct PhaseParams {
     uint16_t* dst;            // up_logits (phase 1) or out (phase 2)
@@ -355,6 +358,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    volatile uint32_t* canary = reinterpret_cast<volatile uint32_t*>(smem + OFF_UNITS + units_bytes(p.num_blocks_m));
+    if (MOE_DEBUG && tid == 0) *canary = SMEM_CANARY;
+    MOE_DCHECK(counts[1] <= p.num_blocks_m && counts[0] <= counts[1], p.status);
     const int32_t tiles1 = PHASE == 2 ? 0 : counts[1] * p.ph[0].n_tiles;
     const int32_t total_tiles = PHASE == 1 ? tiles1
                               : PHASE == 2 ? counts[1] * p.ph[1].n_tiles
@@ -406,6 +412,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 const PhaseParams& pp = p.ph[pt.ph - 1];
                 const Tile ti = decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank);
                 const int32_t e = e_cur;
+                MOE_DCHECK(ti.u >= 0 && ti.u < counts[1] && ti.n >= 0 && ti.n < pp.n_tiles, p.status);
+                MOE_DCHECK(ti.bx >= 0 && ti.bx < p.num_blocks_m && e >= 0 && e < p.n_experts, p.status);
+                MOE_DCHECK(e == __ldg(p.gidx + ti.bx), p.status);
+                MOE_DCHECK(pt.ph == 1 ? ti.n * 128 + 128 <= p.ph[0].n_extent
+                                      : ti.n * BN + static_cast<int32_t>(rank) * 128 < p.ph[1].n_extent,
+                           p.status);
                 const CUtensorMap* a_map = pt.ph == 1 ? &map_x : &map_u;
                 const CUtensorMap* a16_map = pt.ph == 1 ? &map_x16 : &map_u16;
                 if (PHASE == 3 && pt.ph == 2) {
@@ -446,6 +458,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 const uint32_t bytes_peer =
                     !leader ? 0u : ti.pair ? a_bytes(a_boxes(ti.bx0 + 1)) : static_cast<uint32_t>(A_BOX_BYTES);
                 const uint32_t stage_tx = KSUB * (a_bytes(boxes_own) + bytes_peer + 2 * B_BOX_BYTES);
+                MOE_DCHECK(a_row == p.rows_total || static_cast<int64_t>(a_row) + BM <= p.rows_total, p.status);
+                MOE_DCHECK(boxes_own >= 0 && boxes_own <= SMALL_ROWS / 16, p.status);
                 for (int32_t kb = 0; kb < pp.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -558,8 +572,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
             const int64_t grow = static_cast<int64_t>(ti.bx) * BM + row;
+            MOE_DCHECK(actual >= 0 && actual <= BM && (!ti.store || grow < p.rows_total), p.status);
+            MOE_DCHECK(!ti.pair || actual == 0 || __ldg(p.gidx + ti.bx0) == __ldg(p.gidx + ti.bx), p.status);
             if (pt.ph == 1) {
                 uint16_t* dst_row = pp.dst + grow * pp.n_extent + static_cast<int64_t>(ti.n) * 128;
+                MOE_DCHECK(ti.n * 128 + 128 <= pp.n_extent, p.status);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t g[32], u[32];
@@ -590,6 +607,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     const int32_t col0 = ti.n * BN + c * 32;
+                    MOE_DCHECK(col0 >= pp.n_extent || col0 + 32 <= pp.n_extent, p.status);
                     if (col0 >= pp.n_extent) break;             // partial last slice of H
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(taddr + c * 32, v);
@@ -633,6 +651,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     // write into its shared memory, arrive on its barriers or use the TMEM.
     cluster_sync_all();
     if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
+    if (MOE_DEBUG && tid == 0) MOE_DCHECK(*canary == SMEM_CANARY, p.status);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);

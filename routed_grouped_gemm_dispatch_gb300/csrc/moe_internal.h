@@ -4,6 +4,17 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+// MOE_DEBUG builds (-DMOE_DEBUG=1) compile the kernels' own invariant checks;
+// a failed one ORs MOE_DEV_DEBUG_CHECK into the status word and the kernel
+// carries on (no trap).  In release builds the checks compile to nothing.
+#ifndef MOE_DEBUG
+#define MOE_DEBUG 0
+#endif
+#define MOE_DCHECK(cond, status_ptr)                                              \
+    do {                                                                          \
+        if (MOE_DEBUG && !(cond) && (status_ptr)) atomicOr((status_ptr), MOE_DEV_DEBUG_CHECK); \
+    } while (0)
+
 namespace moe {
 
 struct ForwardArgs {

@@ -131,6 +131,8 @@ __global__ void place_pairs_kernel(const int32_t* __restrict__ topk_ids, const f
         }
         return;
     }
+    // the pair lands inside its expert's padded range, before the padding rows
+    MOE_DCHECK(row < __ldg(padded + e + 1) && rank >= 0, status);
     if (lane == 0) {
         pair_rows[f] = static_cast<int32_t>(row);
         if (rw_compact) rw_compact[compact] = __ldg(topk_weights + f);

@@ -209,6 +209,9 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
 #pragma unroll
                 for (int q = 0; q < R_MAX_TOPK; ++q) {
                     if (q < p.top_k) {
+                        // ids in range and the list in descending order
+                        MOE_DCHECK(best_i[q] >= 0 && best_i[q] < p.n_experts, p.status);
+                        MOE_DCHECK(q == 0 || !(best_v[q] > best_v[q > 0 ? q - 1 : 0]), p.status);
                         p.topk_ids[t * p.top_k + q] = best_i[q];
                         p.topk_weights[t * p.top_k + q] = expf(best_v[q] - mx) / s;
                     }

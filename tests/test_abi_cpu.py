@@ -107,3 +107,6 @@ def test_binding_limits_match_header():
     assert defs["MOE_MAX_BLOCKS"] == moe.MAX_BLOCKS
     assert defs["MOE_ROUTER_MAX_EXPERTS"] == moe.ROUTER_MAX_EXPERTS
     assert defs["MOE_ROUTER_MAX_TOPK"] == moe.ROUTER_MAX_TOPK
+    bits = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define (MOE_DEV_\w+)\s+0x([0-9a-fA-F]+)", text)}
+    assert bits == {"MOE_DEV_BAD_EXPERT_ID": moe.MOE_DEV_BAD_EXPERT_ID, "MOE_DEV_BAD_TABLE": moe.MOE_DEV_BAD_TABLE,
+                    "MOE_DEV_TIMEOUT": moe.MOE_DEV_TIMEOUT, "MOE_DEV_DEBUG_CHECK": moe.MOE_DEV_DEBUG_CHECK}
