@@ -76,6 +76,22 @@ def test_small_shapes_full_parity(shape):
     _full_parity(raw_inputs(w, seed=1))
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_random_shapes_full_parity(seed):
+    """Seeded random shapes: 1-64 experts, top-1..8, 1-600 tokens, H and I in
+    128..640, uniform or Zipf routing; every element against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    E = int(rng.choice([1, 2, 3, 5, 8, 16, 40, 64]))
+    k = int(rng.integers(1, min(8, E) + 1))
+    T = int(rng.choice([1, 7, 64, 129, 255, 600]))
+    H = int(rng.choice([128, 256, 384, 640]))
+    I = int(rng.choice([128, 256, 512, 640]))
+    routing = "zipf" if rng.random() < 0.5 else "uniform"
+    w = small_workload(tokens=T, top_k=k, experts=E, hidden=H, intermediate=I, routing=routing,
+                       zipf_s=1.1 if routing == "zipf" else 0.0)
+    _full_parity(raw_inputs(w, seed=seed))
+
+
 def test_exact_multiple_of_block():
     """An expert with exactly 128 rows: the +1 rule gives it a second block,
     which is empty and must be skipped."""
