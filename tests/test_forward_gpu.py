@@ -148,6 +148,26 @@ def test_repeated_calls_identical():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_side_stream_and_concurrent_calls():
+    """The whole chain on a caller's stream, and two independent forwards on two
+    streams at once, give the default-stream result bit for bit."""
+    raw1 = raw_inputs(small_workload(tokens=300, top_k=2, experts=3), seed=4)
+    raw2 = raw_inputs(small_workload(tokens=200, top_k=4, experts=16, hidden=384, intermediate=256), seed=5)
+    side1, side2 = gpu_prepare(raw1), gpu_prepare(raw2)
+    ref1 = [bits(t) for t in run_forward(side1, raw1.w.intermediate)]
+    ref2 = [bits(t) for t in run_forward(side2, raw2.w.intermediate)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        got1 = run_forward(side1, raw1.w.intermediate)
+    with torch.cuda.stream(s2):
+        got2 = run_forward(side2, raw2.w.intermediate)
+    torch.cuda.synchronize()
+    assert all(np.array_equal(bits(g), r) for g, r in zip(got1, ref1))
+    assert all(np.array_equal(bits(g), r) for g, r in zip(got2, ref2))
+
+
 # --------------------------------------------------------------------------
 # full-size workloads: sampled rows
 # --------------------------------------------------------------------------
