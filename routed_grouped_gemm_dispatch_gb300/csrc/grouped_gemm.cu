@@ -187,6 +187,54 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Epilogue stores in whole 128-byte lines.  Each thread holds 64 fp16 columns
+// of its own row as eight 16-byte pieces.  Inside every group of 8 lanes the
+// 8 x 8 grid of pieces is transposed with three rounds of butterfly shuffles
+// (round m swaps the pieces whose index bit m differs from the lane's bit m),
+// after which lane 8g + i holds piece i of rows 8g .. 8g + 7; one store per
+// row then writes a full 128-byte line from 8 lanes, 4 lines per warp
+// instruction, instead of 32 half-filled sectors.
+__device__ __forceinline__ void transpose8_pieces(uint4 (&el)[8], int lane) {
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+        const bool hi = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (e & m) continue;
+            const int f = e | m;
+            const uint4 send = hi ? el[e] : el[f];
+            uint4 recv;
+            recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+            recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+            recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+            recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+            if (hi) el[e] = recv;
+            else el[f] = recv;
+        }
+    }
+}
+
+// Store the 64 columns the warp's threads hold for their rows (el[k] = columns
+// 8k .. 8k+7 of row warp_row0 + lane), rows below `actual` only.  `dst0`
+// points at the first column in row warp_row0; `stride` is the row stride.
+// A warp with at least 16 valid rows transposes first and writes whole lines;
+// a sparser warp (decode-like blocks) stores each thread's row directly.
+__device__ __forceinline__ void store_rows64(uint4 (&el)[8], uint16_t* dst0, int64_t stride, int lane,
+                                            int warp_row0, int32_t actual) {
+    if (warp_row0 + 16 <= actual) {
+        transpose8_pieces(el, lane);
+        const int g8 = lane & ~7;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            if (warp_row0 + g8 + r < actual)
+                *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(g8 + r) * stride + (lane & 7) * 8) = el[r];
+    } else if (warp_row0 + lane < actual) {
+        uint4* d = reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(lane) * stride);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) d[k] = el[k];
+    }
+}
+
 // Which phase a tile of the launch belongs to, and its index inside that
 // phase.  PHASE 1 or 2 launches run one phase; PHASE 3 runs both: the first
 // nunits * n_tiles(phase 1) tiles are phase 1, the rest phase 2.
@@ -574,11 +622,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const int64_t grow = static_cast<int64_t>(ti.bx) * BM + row;
             MOE_DCHECK(actual >= 0 && actual <= BM && (!ti.store || grow < p.rows_total), p.status);
             MOE_DCHECK(!ti.pair || actual == 0 || __ldg(p.gidx + ti.bx0) == __ldg(p.gidx + ti.bx), p.status);
+            // rows [warp_row0, warp_row0 + 32) of the block are this warp's
+            const int warp_row0 = quarter * 32;
+            const int64_t wrow = static_cast<int64_t>(ti.bx) * BM + warp_row0;
             if (pt.ph == 1) {
                 uint16_t* dst_row = pp.dst + grow * pp.n_extent + static_cast<int64_t>(ti.n) * 128;
                 MOE_DCHECK(ti.n * 128 + 128 <= pp.n_extent, p.status);
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < (warp_row0 < actual ? 4 : 0); ++c) {
                     uint32_t g[32], u[32];
                     tmem_ld_32x32b_x32(taddr + c * 32, g);
                     tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
@@ -603,25 +654,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             } else {
                 float w = 0.0f;
                 if (row < actual) w = __ldg(p.rw + (__ldg(p.offsets + e) + tok + row));
-                uint16_t* dst_row = pp.dst + grow * pp.n_extent;
+                uint16_t* dst0 = pp.dst + wrow * pp.n_extent;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < (warp_row0 < actual ? BN / 32 : 0); c += 2) {   // 64 columns per pass
                     const int32_t col0 = ti.n * BN + c * 32;
-                    MOE_DCHECK(col0 >= pp.n_extent || col0 + 32 <= pp.n_extent, p.status);
+                    MOE_DCHECK(col0 >= pp.n_extent || col0 + 64 <= pp.n_extent, p.status);
                     if (col0 >= pp.n_extent) break;             // partial last slice of H
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, v);
-                    tmem_ld_wait();
-                    if (row < actual) {
+                    uint4 el[8];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr + (c + half) * 32, v);
+                        tmem_ld_wait();
                         uint32_t h[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             h[j] = pack_half2(__uint_as_float(v[2 * j]) * w, __uint_as_float(v[2 * j + 1]) * w);
-                        uint4* d4 = reinterpret_cast<uint4*>(dst_row + col0);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            d4[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                            el[4 * half + q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
                     }
+                    store_rows64(el, dst0 + col0, pp.n_extent, lane, warp_row0, actual);
                 }
             }
             tc_fence_before_sync();
