@@ -12,8 +12,8 @@ working set (1.45 GB) is far larger than the 129 MB L2, so back-to-back steps
 do not reuse L2 between iterations.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-instead (the reference arm for this build: the pages' own kernel targets a
-MetaX C500 and cannot run here).
+instead (the reference arm: the pages' own kernel targets a MetaX C500 and
+cannot run on this GPU).
 
 Multi-GPU: the path does not shard inside one forward on one GPU; N ranks run
 independent replicas of the workload ("replicas only"), value = units of all

@@ -5,7 +5,7 @@ into ``_build/libmoe_gb300.so``.  Rebuilds only when a source is newer than
 the library.  ``build(debug=True)`` makes ``_build/libmoe_gb300_debug.so`` with
 ``-DMOE_DEBUG=1``: the kernels then also check their own indices, coordinates
 and shared-memory layout and report a failed check as MOE_DEV_DEBUG_CHECK in
-the status word (the stand-in for a sanitizer, which this pool does not run).
+the status word (the stand-in for a sanitizer where none can run).
 """
 from __future__ import annotations
 

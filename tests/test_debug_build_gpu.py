@@ -1,4 +1,4 @@
-"""The MOE_DEBUG build, the stand-in for a sanitizer on this pool: its kernels
+"""The MOE_DEBUG build, the stand-in for a sanitizer where none can run: its kernels
 also check their own tile indices, TMA coordinates, store bounds, table
 invariants and a shared-memory canary, and report a failed check as
 MOE_DEV_DEBUG_CHECK.  On every case of debug_build_cases.py it raises no check
