@@ -45,6 +45,10 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     // A forward launched right behind this kernel may start its own set-up
     // now; it reads the tables only after this grid has completed.
     pdl_launch_dependents();
+    // This kernel is itself launched with programmatic dependent launch, so
+    // it may start during the tail of the previous kernel on the stream (for
+    // example the previous step's phase 2, which still reads the tables):
+    // counting reads only topk_ids; every global write waits for that kernel.
     for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
     __syncthreads();
 
@@ -81,6 +85,7 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
         done = 4 * n4;
     }
     for (int64_t f = done + tid; f < pairs; f += DISPATCH_THREADS) count(__ldg(topk_ids + f));
+    pdl_wait_prior_grid();
     if (bad && status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
 
@@ -144,9 +149,18 @@ cudaError_t launch_build_dispatch(const int32_t* topk_ids, int64_t pairs, int32_
                                   int32_t block_token, int32_t* sizes, int32_t* offsets,
                                   int32_t* padded, int32_t* gidx, int64_t num_blocks_m,
                                   int32_t* status, cudaStream_t stream) {
-    build_dispatch_kernel<<<1, DISPATCH_THREADS, 0, stream>>>(topk_ids, pairs, n_experts, block_token, sizes,
-                                                              offsets, padded, gidx, num_blocks_m, status);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(DISPATCH_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, build_dispatch_kernel, topk_ids, pairs, n_experts, block_token, sizes, offsets,
+                              padded, gidx, num_blocks_m, status);
 }
 
 }  // namespace moe

@@ -345,7 +345,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     // Phase 2 directly behind phase 1 may read the dispatch tables earlier
     // (phase 1 only lets it start once phase 1 itself has waited).
     if (PHASE != 2 || !p.tables_before_wait) pdl_wait_prior_grid();
-    if (PHASE == 1) pdl_launch_dependents();
+    // Let the next kernel on the stream launch: phase 2 behind phase 1, or
+    // the next step's table builder behind phase 2 (it waits for this grid
+    // before it writes anything).
+    pdl_launch_dependents();
 
     // ---- 1. compacted list of active blocks and their experts (bx order) ---
     int32_t nact = 0;
