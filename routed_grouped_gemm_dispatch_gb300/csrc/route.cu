@@ -138,16 +138,32 @@ __global__ void place_pairs_kernel(const int32_t* __restrict__ topk_ids, const f
         if (rw_compact) rw_compact[compact] = __ldg(topk_weights + f);
     }
     if (x_packed) {
+        // eight 16-byte loads in flight per lane before their stores
         const uint4* src = reinterpret_cast<const uint4*>(x_tokens + (f / top_k) * static_cast<int64_t>(hidden));
         uint4* dst = reinterpret_cast<uint4*>(x_packed + row * static_cast<int64_t>(hidden));
-        for (int32_t i = lane; i < hidden / 8; i += 32) dst[i] = __ldg(src + i);
+        const int32_t n16 = hidden / 8;
+        for (int32_t i0 = 0; i0 < n16; i0 += 8 * 32) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int32_t i = i0 + u * 32 + lane;
+                if (i < n16) v[u] = __ldg(src + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int32_t i = i0 + u * 32 + lane;
+                if (i < n16) dst[i] = v[u];
+            }
+        }
     }
 }
 
 constexpr int COMBINE_THREADS = 256;
 
 // One CTA per token; each thread sums 8 consecutive columns of the token's k
-// expert rows in j order.
+// expert rows in j order, with up to JB rows' loads in flight before the sums
+// (JB follows top_k, so a small k keeps few registers and many CTAs per SM).
+template <int JB>
 __global__ void __launch_bounds__(COMBINE_THREADS)
 combine_kernel(const uint16_t* __restrict__ out, int64_t rows_total, int32_t hidden,
                const int32_t* __restrict__ pair_rows, int32_t top_k, uint16_t* __restrict__ y) {
@@ -156,16 +172,26 @@ combine_kernel(const uint16_t* __restrict__ out, int64_t rows_total, int32_t hid
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int32_t j = 0; j < top_k; ++j) {
-            const int64_t row = __ldg(pair_rows + t * top_k + j);
-            if (row < 0 || row >= rows_total) continue;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(out + row * hidden) + c8);
-            const __half2* h = reinterpret_cast<const __half2*>(&v);
+        for (int32_t j0 = 0; j0 < top_k; j0 += JB) {
+            uint4 v[JB];
+            bool ok[JB];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f2 = __half22float2(h[i]);
-                acc[2 * i] += f2.x;
-                acc[2 * i + 1] += f2.y;
+            for (int u = 0; u < JB; ++u) {
+                const int32_t j = j0 + u;
+                const int64_t row = j < top_k ? static_cast<int64_t>(__ldg(pair_rows + t * top_k + j)) : -1;
+                ok[u] = row >= 0 && row < rows_total;
+                if (ok[u]) v[u] = __ldg(reinterpret_cast<const uint4*>(out + row * hidden) + c8);
+            }
+#pragma unroll
+            for (int u = 0; u < JB; ++u) {
+                if (!ok[u]) continue;
+                const __half2* h = reinterpret_cast<const __half2*>(&v[u]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f2 = __half22float2(h[i]);
+                    acc[2 * i] += f2.x;
+                    acc[2 * i + 1] += f2.y;
+                }
             }
         }
         uint4 o;
@@ -212,8 +238,13 @@ cudaError_t launch_pack(const int32_t* topk_ids, const float* topk_weights, int6
 cudaError_t launch_combine(const uint16_t* out, int64_t rows_total, int32_t hidden, const int32_t* pair_rows,
                            int64_t n_tokens, int32_t top_k, uint16_t* y, cudaStream_t stream) {
     if (n_tokens == 0) return cudaSuccess;
-    combine_kernel<<<static_cast<unsigned>(n_tokens), COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden,
-                                                                                    pair_rows, top_k, y);
+    const unsigned grid = static_cast<unsigned>(n_tokens);
+    if (top_k <= 2)
+        combine_kernel<2><<<grid, COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden, pair_rows, top_k, y);
+    else if (top_k <= 4)
+        combine_kernel<4><<<grid, COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden, pair_rows, top_k, y);
+    else
+        combine_kernel<8><<<grid, COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden, pair_rows, top_k, y);
     return cudaGetLastError();
 }
 
