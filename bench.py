@@ -409,7 +409,9 @@ def main():
     value = job_value(world, flops, ms)
 
     # ---- per-phase durations (same stream, CUDA events) -------------------
-    n_ph = max(5, min(args.steps, 50))
+    # (enough steps that the power-capped clock settles as in the timed loop;
+    # the second half is averaged)
+    n_ph = max(6, min(args.steps, 500))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ph)]
     for i in range(n_ph):
         e = evs[i]
@@ -425,9 +427,10 @@ def main():
                           d["ul"], d["out"], status=status, flags=moe.MOE_RUN_PHASE2 | moe.MOE_NO_PDL)
         e[3].record()
     torch.cuda.synchronize(dev)
-    dispatch_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    p1_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    p2_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    steady = evs[n_ph // 2:]
+    dispatch_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in steady)
+    p1_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in steady)
+    p2_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in steady)
     dev_status = int(status.item())
 
     # ---- end to end through the public API with host buffers ---------------
