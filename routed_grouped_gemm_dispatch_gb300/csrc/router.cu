@@ -5,11 +5,11 @@
 // One CTA per 128-token tile, one tcgen05 MMA tile of M = 128 tokens and
 // N = n_experts rounded up to 16 (at most 256), so a token's whole logit row
 // sits in one TMEM lane.  Warp 0 streams x and W_g with TMA (4 stages of
-// 64-wide K), warp 1 owns TMEM and issues the MMAs, warps 2-5 each take 32
-// tokens: a register top-k over the row (ties to the lower expert index,
-// written in descending order), then the softmax denominator over all experts
-// against the row maximum.  The top-k is decided on the logits (softmax
-// preserves their order).
+// 64-wide K), warp 1 owns TMEM and issues the MMAs, warps 2-9 split each
+// token's row in two halves of the expert columns: per half a register top-k
+// (ties to the lower expert index, descending order) and the softmax sum
+// against the half's maximum, then the first half's thread merges the two.
+// The top-k is decided on the logits (softmax preserves their order).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -29,15 +29,19 @@ constexpr int R_STAGES = 4;
 constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB
 constexpr int R_B_MAX_BYTES = 256 * R_BK * 2;        // 32 KB
 constexpr int R_STAGE_BYTES = R_A_BYTES + R_B_MAX_BYTES;
-constexpr int R_THREADS = 192;
-constexpr int R_EPI_THREADS = 128;
+constexpr int R_THREADS = 320;                       // producer, MMA, 8 epilogue warps
+constexpr int R_EPI_THREADS = 256;
 constexpr int R_MAX_TOPK = 16;
 constexpr uint64_t R_WAIT_NS = 2000000000ull;
 constexpr uint64_t R_DRAIN_NS = 200000000ull;
 constexpr int R_OFF_BARS = R_STAGES * R_STAGE_BYTES;
 constexpr int R_OFF_TMEM = R_OFF_BARS + (2 * R_STAGES + 2) * 8;
 constexpr int R_OFF_ABORT = R_OFF_TMEM + 4;
-constexpr size_t R_SMEM = 1024 + R_OFF_ABORT + 16;
+// the second half-row's partial results, handed to the first half's thread:
+// top-k values [R_MAX_TOPK][128], ids [R_MAX_TOPK][128], max [128], sum [128]
+constexpr int R_OFF_XCH = ((R_OFF_ABORT + 4 + 15) / 16) * 16;
+constexpr int R_XCH_BYTES = (2 * R_MAX_TOPK + 2) * R_BM * 4;
+constexpr size_t R_SMEM = 1024 + R_OFF_XCH + R_XCH_BYTES;
 
 struct RouterParams {
     int64_t n_tokens;
@@ -148,29 +152,54 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         }
         __syncwarp();
     } else {
+        // Warps 2-9: warp w reads TMEM lanes 32*(w%4) .. +31 (one token per
+        // thread); warps 2-5 take the first half of the expert columns and
+        // warps 6-9 the second half, then the second half's thread hands its
+        // partial top-k, max and sum to the first half's thread of the same
+        // token, which merges them and writes the token's outputs.
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const int64_t t = static_cast<int64_t>(row0) + row;
-        if (mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS)) {
+        const int32_t n_half = p.n_pad / 2;              // a multiple of 8
+        const int32_t c_begin = half * n_half;
+        float* xv = reinterpret_cast<float*>(smem + R_OFF_XCH);
+        int32_t* xi = reinterpret_cast<int32_t*>(xv + R_MAX_TOPK * R_BM);
+        float* xm = reinterpret_cast<float*>(xi + R_MAX_TOPK * R_BM);
+        float* xs = xm + R_BM;
+        float best_v[R_MAX_TOPK];
+        int32_t best_i[R_MAX_TOPK];
+#pragma unroll
+        for (int q = 0; q < R_MAX_TOPK; ++q) {
+            best_v[q] = -INFINITY;
+            best_i[q] = -1;
+        }
+        float s = 0.0f;
+        // Insert (l, e) into the descending list (everything in registers: all
+        // loops over the list are unrolled with compile-time indices).  A new
+        // value goes in after any equal one, so the lower expert index stays
+        // first, and every slot is updated from the old list at once.
+        auto insert = [&](float l, int32_t e) {
+            bool gt[R_MAX_TOPK];
+#pragma unroll
+            for (int q = 0; q < R_MAX_TOPK; ++q) gt[q] = best_i[q] < 0 || l > best_v[q];
+#pragma unroll
+            for (int q = R_MAX_TOPK - 1; q > 0; --q) {
+                best_v[q] = gt[q - 1] ? best_v[q - 1] : (gt[q] ? l : best_v[q]);
+                best_i[q] = gt[q - 1] ? best_i[q - 1] : (gt[q] ? e : best_i[q]);
+            }
+            if (gt[0]) {
+                best_v[0] = l;
+                best_i[0] = e;
+            }
+        };
+        const bool ok = mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS);
+        if (ok) {
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            // Two passes over the row in TMEM, everything in registers (every
-            // loop over a chunk or the list is unrolled with compile-time
-            // indices).  Pass 1 keeps the R_MAX_TOPK largest logits in a
-            // descending list: a new value goes in after any equal one (the
-            // lower expert index stays first), and every slot is updated from
-            // the old list at once instead of by a serial walk.  Pass 2 sums
-            // exp(l - max) with independent partial sums.
-            float best_v[R_MAX_TOPK];
-            int32_t best_i[R_MAX_TOPK];
-#pragma unroll
-            for (int q = 0; q < R_MAX_TOPK; ++q) {
-                best_v[q] = -INFINITY;
-                best_i[q] = -1;
-            }
-            // (8 columns per TMEM load keeps the unrolled insertion code small
-            // enough for the instruction cache)
-            for (int32_t c0 = 0; c0 < p.n_pad; c0 += 8) {
+            // pass 1: the R_MAX_TOPK largest logits of this half (8 columns per
+            // TMEM load keeps the unrolled code within the instruction cache)
+            for (int32_t c0 = c_begin; c0 < c_begin + n_half; c0 += 8) {
                 uint32_t v[8];
                 tmem_ld_32x32b_x8(taddr + c0, v);
                 tmem_ld_wait();
@@ -178,33 +207,46 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                 for (int j = 0; j < 8; ++j) {
                     const int32_t e = c0 + j;
                     const float l = __uint_as_float(v[j]);
-                    if (e < p.n_experts && (best_i[R_MAX_TOPK - 1] < 0 || l > best_v[R_MAX_TOPK - 1])) {
-                        bool gt[R_MAX_TOPK];
-#pragma unroll
-                        for (int q = 0; q < R_MAX_TOPK; ++q) gt[q] = best_i[q] < 0 || l > best_v[q];
-#pragma unroll
-                        for (int q = R_MAX_TOPK - 1; q > 0; --q) {
-                            best_v[q] = gt[q - 1] ? best_v[q - 1] : (gt[q] ? l : best_v[q]);
-                            best_i[q] = gt[q - 1] ? best_i[q - 1] : (gt[q] ? e : best_i[q]);
-                        }
-                        if (gt[0]) {
-                            best_v[0] = l;
-                            best_i[0] = e;
-                        }
-                    }
+                    if (e < p.n_experts && (best_i[R_MAX_TOPK - 1] < 0 || l > best_v[R_MAX_TOPK - 1])) insert(l, e);
                 }
             }
-            const float mx = best_v[0];
+            // pass 2: sum of exp(l - this half's max), independent partial sums
+            const float mh = best_v[0];
             float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            for (int32_t c0 = 0; c0 < p.n_pad; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + c0, v);
+            for (int32_t c0 = c_begin; c0 < c_begin + n_half; c0 += 8) {
+                uint32_t v[8];
+                tmem_ld_32x32b_x8(taddr + c0, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < p.n_experts) part[j & 3] += expf(__uint_as_float(v[j]) - mx);
+                for (int j = 0; j < 8; ++j)
+                    if (c0 + j < p.n_experts) part[j & 3] += expf(__uint_as_float(v[j]) - mh);
             }
-            const float s = (part[0] + part[1]) + (part[2] + part[3]);
+            s = (part[0] + part[1]) + (part[2] + part[3]);
+            if (half == 1) {
+#pragma unroll
+                for (int q = 0; q < R_MAX_TOPK; ++q) {
+                    xv[q * R_BM + row] = best_v[q];
+                    xi[q * R_BM + row] = best_i[q];
+                }
+                xm[row] = mh;
+                xs[row] = s;
+            }
+        }
+        // every epilogue thread meets here, whatever its wait returned
+        asm volatile("bar.sync 1, %0;" ::"r"(R_EPI_THREADS) : "memory");
+        if (half == 0 && ok && !*abort_flag) {
+            // merge: the other half's experts all have higher indices, so its
+            // entries go after equal values already in the list
+            const float m0 = best_v[0], m1 = xm[row];
+            for (int q = 0; q < R_MAX_TOPK; ++q) {
+                const int32_t e = xi[q * R_BM + row];
+                const float l = xv[q * R_BM + row];
+                if (e < 0) break;
+                if (best_i[R_MAX_TOPK - 1] >= 0 && !(l > best_v[R_MAX_TOPK - 1])) break;
+                insert(l, e);
+            }
+            const float mx = best_v[0];                   // = max(m0, m1)
+            const float st = s * expf(m0 - mx) + (m1 == -INFINITY ? 0.0f : xs[row] * expf(m1 - mx));
             if (t < p.n_tokens) {
 #pragma unroll
                 for (int q = 0; q < R_MAX_TOPK; ++q) {
@@ -213,7 +255,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                         MOE_DCHECK(best_i[q] >= 0 && best_i[q] < p.n_experts, p.status);
                         MOE_DCHECK(q == 0 || !(best_v[q] > best_v[q > 0 ? q - 1 : 0]), p.status);
                         p.topk_ids[t * p.top_k + q] = best_i[q];
-                        p.topk_weights[t * p.top_k + q] = expf(best_v[q] - mx) / s;
+                        p.topk_weights[t * p.top_k + q] = expf(best_v[q] - mx) / st;
                     }
                 }
             }
