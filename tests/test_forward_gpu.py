@@ -148,6 +148,25 @@ def test_repeated_calls_identical():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_phases_run_separately_match_the_fused_call():
+    """moe_fused_forward_ex: phase 1 alone, then phase 2 alone (with and without
+    programmatic dependent launch), reproduces the two-phase call bit for bit."""
+    raw = raw_inputs(small_workload(tokens=500, top_k=4, experts=40, hidden=384, intermediate=256), seed=6)
+    side = gpu_prepare(raw)
+    ref = [bits(t) for t in run_forward(side, raw.w.intermediate)]
+    from gpu_side import sentinel
+    t = side.tables
+    for p2_flags in (moe.MOE_RUN_PHASE2, moe.MOE_RUN_PHASE2 | moe.MOE_NO_PDL):
+        ul = sentinel(side.rows_total, raw.w.intermediate)
+        out = sentinel(side.rows_total, raw.w.hidden)
+        for flags in (moe.MOE_RUN_PHASE1, p2_flags):
+            moe.fused_forward(side.x_packed, side.gate, side.up, side.down, side.rw, t["group_sizes"],
+                              t["group_offsets"], t["group_padded_offsets"], t["group_idx_for_bx"], ul, out,
+                              flags=flags)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(ul), ref[0]) and np.array_equal(bits(out), ref[1])
+
+
 def test_side_stream_and_concurrent_calls():
     """The whole chain on a caller's stream, and two independent forwards on two
     streams at once, give the default-stream result bit for bit."""
