@@ -21,7 +21,7 @@
  *        §1.12.1 and §2.4 (gate = SiLU(x W_gate), up = x W_up, mid = gate*up,
  *        out = mid W_down; the router: logits = W_g(x), softmax, top-k).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - fp32 -> fp16 conversion is IEEE-754 round-to-nearest-even, overflow to inf.
  *   - group_offsets and group_padded_offsets hold E+1 entries; entry E is the
  *     total number of pairs / padded rows.
