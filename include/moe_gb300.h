@@ -264,7 +264,10 @@ moe_status_t moe_fused_forward_single_launch(
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The cache does not survive a
+ *     device reset: do not use this call across cudaDeviceReset.
+ *   - Argument checks: first the ones moe_fused_forward makes (same codes,
+ *     same order), then the workspace limit (MOE_ERR_STATIC_WORKSPACE).
  *   - All calls in the process share the one array per device and it keeps
  *     the last call's contents.  Nothing in it has to start at zero.  Calls
  *     whose kernels overlap on the GPU (different streams, no ordering between

@@ -47,9 +47,12 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     pdl_launch_dependents();
     // This kernel is itself launched with programmatic dependent launch, so
     // it may start during the tail of the previous kernel on the stream (for
-    // example the previous step's phase 2, which still reads the tables):
-    // counting reads only topk_ids; every global write waits for that kernel.
+    // example the previous step's phase 2, which still reads the tables, or a
+    // router that writes topk_ids).  Only the shared-memory set-up overlaps
+    // that kernel: griddepcontrol.wait is the one point after which its
+    // writes are visible, so every global read and write comes after it.
     for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
+    pdl_wait_prior_grid();
     __syncthreads();
 
     // histogram of the flattened expert ids: 16-byte loads, eight per thread
@@ -85,7 +88,6 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
         done = 4 * n4;
     }
     for (int64_t f = done + tid; f < pairs; f += DISPATCH_THREADS) count(__ldg(topk_ids + f));
-    pdl_wait_prior_grid();
     if (bad && status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
 

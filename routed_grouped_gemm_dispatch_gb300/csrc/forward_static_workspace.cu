@@ -14,13 +14,17 @@
 // library's module is loaded holds it (STATIC_UP_LOGITS_BYTES) until the
 // process exits.  In host code its name is only a host-side stand-in, so the
 // device address is looked up with cudaGetSymbolAddress, once per device with
-// that device current, on the first call made on that device.
+// that device current, on the first call made on that device, and cached.
+// The cache is not told about a device reset: after cudaDeviceReset (or any
+// re-creation of the device's primary context) the cached address is stale,
+// so this entry point must not be used across a reset.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/moe_gb300.h"
+#include "moe_internal.h"
 
 namespace {
 
@@ -40,7 +44,10 @@ void* static_workspace_address() {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (g_addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_up_logits) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_up_logits) != cudaSuccess) {
+            cudaGetLastError();   // leave no pending error behind for the caller's next check
+            return nullptr;
+        }
         g_addr[dev] = p;
     }
     return g_addr[dev];
@@ -55,7 +62,26 @@ extern "C" moe_status_t moe_fused_forward_static_workspace(
     const int32_t* group_sizes, const int32_t* group_offsets, const int32_t* group_padded_offsets,
     const int32_t* group_idx_for_bx, int64_t num_blocks_m, uint16_t* out, int32_t* status_dev,
     void* stream) {
-    if (total_padded_tokens < 0 || intermediate <= 0) return MOE_ERR_SHAPE;
+    // The checks every forward makes come first (same codes, same order as
+    // moe_fused_forward), then the limit of the fixed workspace.
+    moe::ForwardArgs a{};
+    a.x = stacked_expert_tokens;
+    a.rows_total = total_padded_tokens;
+    a.hidden = hidden;
+    a.gate_w = gate_w;
+    a.up_w = up_w;
+    a.down_w = down_w;
+    a.n_experts = n_experts;
+    a.intermediate = intermediate;
+    a.rw = routed_expert_weights;
+    a.valid_total = total_valid_tokens;
+    a.sizes = group_sizes;
+    a.offsets = group_offsets;
+    a.padded = group_padded_offsets;
+    a.gidx = group_idx_for_bx;
+    a.num_blocks_m = num_blocks_m;
+    a.out = out;
+    if (moe_status_t s = moe::check_forward_args(a, false)) return s;
     const double need = static_cast<double>(total_padded_tokens) * intermediate * sizeof(uint16_t);
     if (need > static_cast<double>(STATIC_UP_LOGITS_BYTES)) return MOE_ERR_STATIC_WORKSPACE;
     void* ws = static_workspace_address();

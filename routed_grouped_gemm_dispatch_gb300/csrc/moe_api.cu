@@ -140,6 +140,26 @@ moe_status_t moe_router_topk(const uint16_t* x_tokens, int64_t n_tokens, int32_t
 
 }  // extern "C"
 
+namespace moe {
+
+int32_t check_forward_args(const ForwardArgs& a, bool check_up_logits) {
+    if (!a.x || !a.gate_w || !a.up_w || !a.down_w || (a.valid_total > 0 && !a.rw) || !a.sizes || !a.offsets ||
+        !a.padded || !a.gidx || (check_up_logits && !a.up_logits) || !a.out)
+        return MOE_ERR_NULL;
+    if (a.hidden <= 0 || a.intermediate <= 0 || a.hidden % 128 != 0 || a.intermediate % 128 != 0)
+        return MOE_ERR_SHAPE;
+    if (a.rows_total < 0 || a.valid_total < 0 || a.num_blocks_m < 0) return MOE_ERR_SHAPE;
+    if (a.n_experts <= 0 || a.n_experts > MOE_MAX_EXPERTS) return MOE_ERR_LIMIT;
+    if (a.num_blocks_m > MOE_MAX_BLOCKS) return MOE_ERR_LIMIT;
+    if (a.rows_total < a.num_blocks_m * MOE_BLOCK_TOKEN) return MOE_ERR_SHAPE;
+    if (!aligned16(a.x) || !aligned16(a.gate_w) || !aligned16(a.up_w) || !aligned16(a.down_w) ||
+        (check_up_logits && !aligned16(a.up_logits)) || !aligned16(a.out))
+        return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+}  // namespace moe
+
 namespace {
 
 moe_status_t forward_impl(const uint16_t* stacked_expert_tokens, int64_t total_padded_tokens, int32_t hidden,
@@ -152,22 +172,6 @@ moe_status_t forward_impl(const uint16_t* stacked_expert_tokens, int64_t total_p
     const uint32_t phases = flags & (MOE_RUN_PHASE1 | MOE_RUN_PHASE2);
     if (phases == 0 || (flags & ~(MOE_RUN_PHASE1 | MOE_RUN_PHASE2 | MOE_NO_PDL | MOE_TEST_DROP_SIGNAL)) != 0)
         return MOE_ERR_SHAPE;
-    if (!stacked_expert_tokens || !gate_w || !up_w || !down_w ||
-        (total_valid_tokens > 0 && !routed_expert_weights) || !group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx || !up_logits ||
-        !out)
-        return MOE_ERR_NULL;
-    if (hidden <= 0 || intermediate <= 0 || hidden % 128 != 0 || intermediate % 128 != 0)
-        return MOE_ERR_SHAPE;
-    if (total_padded_tokens < 0 || total_valid_tokens < 0 || num_blocks_m < 0) return MOE_ERR_SHAPE;
-    if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return MOE_ERR_LIMIT;
-    if (num_blocks_m > MOE_MAX_BLOCKS) return MOE_ERR_LIMIT;
-    if (total_padded_tokens < num_blocks_m * MOE_BLOCK_TOKEN) return MOE_ERR_SHAPE;
-    if (!aligned16(stacked_expert_tokens) || !aligned16(gate_w) || !aligned16(up_w) ||
-        !aligned16(down_w) || !aligned16(up_logits) || !aligned16(out))
-        return MOE_ERR_ALIGN;
-    if (moe_status_t s = check_device()) return s;
-    if (num_blocks_m == 0) return MOE_OK;
-
     moe::ForwardArgs a{};
     a.x = stacked_expert_tokens;
     a.rows_total = total_padded_tokens;
@@ -187,6 +191,9 @@ moe_status_t forward_impl(const uint16_t* stacked_expert_tokens, int64_t total_p
     a.up_logits = up_logits;
     a.out = out;
     a.status = status_dev;
+    if (moe_status_t s = moe::check_forward_args(a, true)) return s;
+    if (moe_status_t s = check_device()) return s;
+    if (num_blocks_m == 0) return MOE_OK;
     return from_cuda(moe::launch_fused_forward(a, flags, static_cast<cudaStream_t>(stream), ready_ws));
 }
 

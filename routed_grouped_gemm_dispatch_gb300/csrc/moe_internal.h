@@ -38,6 +38,12 @@ struct ForwardArgs {
     int32_t* status;
 };
 
+// Host-side checks shared by the forward entry points: NULL pointers,
+// shapes, library limits, padded row count and 16-byte alignment, in that
+// order; the up_logits pointer only when `check_up_logits`.  Returns MOE_OK or
+// the first MOE_ERR_* that applies.  No device call.
+int32_t check_forward_args(const ForwardArgs& a, bool check_up_logits);
+
 // Enqueue the dispatch-table builder.  Arguments already validated.
 cudaError_t launch_build_dispatch(const int32_t* topk_ids, int64_t pairs, int32_t n_experts,
                                   int32_t block_token, int32_t* sizes, int32_t* offsets,

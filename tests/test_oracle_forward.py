@@ -239,3 +239,63 @@ def test_pack_and_combine_closed_forms(small):
             out[side.pair_rows[t, j]] = 0.25 * (j + 1)
     y = oracle.combine(out.view(np.uint16), side.pair_rows, T, k).view(np.float16)
     assert np.all(y == np.float16(0.25 * k * (k + 1) / 2))
+
+
+def _combine_case(T, k, H, rng, values):
+    """Pair rows scattered over a padded array: token t's j-th row holds
+    values[t, j] (fp16 [T, k, H]); every other row is NaN."""
+    rows_total = 4 * T * k + 7
+    pr = rng.permutation(rows_total)[:T * k].astype(np.int32).reshape(T, k)
+    out = np.full((rows_total, H), np.nan, np.float16)
+    for t in range(T):
+        for j in range(k):
+            out[pr[t, j]] = values[t, j]
+    return out, pr
+
+
+def test_combine_pinned_by_exact_sums():
+    """oracle.combine against the exact sum rounded once to fp16 (numpy's
+    float64 sum, then numpy's RNE cast): "MetaX-TileLang工具链" §2.7 sums a
+    token's expert rows with scatter_reduce; the reading is an fp32 sum in j
+    order with one rounding.  The row values are distinct per (token, j) and
+    are multiples of 2^-6 below 2^5 in magnitude, so every partial sum of up
+    to 8 of them is exact in fp32 and the exact sum is the reference: a
+    combine that reads another token's rows or another j, drops a row, or
+    rounds a partial sum to fp16 fails."""
+    rng = np.random.default_rng(11)
+    T, k, H = 37, 6, 64
+    vals = (rng.integers(-2047, 2048, size=(T, k, H)) / 64.0).astype(np.float16)
+    assert np.all(vals.astype(np.float64) * 64 == np.round(vals.astype(np.float64) * 64))
+    out, pr = _combine_case(T, k, H, rng, vals)
+    y = oracle.combine(out.view(np.uint16), pr, T, k).view(np.float16)
+    expect = vals.astype(np.float64).sum(axis=1).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), expect.view(np.uint16))
+    # the values really tell tokens and rows apart (the pin would catch a mix-up)
+    swapped = vals[::-1].astype(np.float64).sum(axis=1).astype(np.float16)
+    assert not np.array_equal(swapped, expect)
+    fewer = vals[:, :-1].astype(np.float64).sum(axis=1).astype(np.float16)
+    assert np.count_nonzero(fewer != expect) > 0.9 * expect.size
+
+
+def test_combine_special_sums():
+    """Cancellation to +0, a sum an fp16 accumulator would get wrong
+    (2048 + 1 + 1: fp16 steps are 2 above 2048, so rounding each partial sum
+    gives 2048, the fp32 sum gives 2050), and overflow: a sum at or above
+    65520 rounds to +inf under round-to-nearest-even, 65519 to 65504."""
+    rng = np.random.default_rng(12)
+    cases = [
+        ([1000.5, -1000.5, 3.25, -3.25], 0.0),
+        ([2048.0, 1.0, 1.0, 0.0], 2050.0),
+        ([30000.0, 30000.0, 5520.0, 0.0], np.inf),
+        ([-30000.0, -30000.0, -5520.0, 0.0], -np.inf),
+        ([30000.0, 30000.0, 5504.0, 15.0], 65504.0),
+    ]
+    T, k, H = len(cases), 4, 8
+    vals = np.zeros((T, k, H), np.float16)
+    for t, (v, _) in enumerate(cases):
+        vals[t] = np.array(v, np.float16)[:, None]
+    out, pr = _combine_case(T, k, H, rng, vals)
+    y = oracle.combine(out.view(np.uint16), pr, T, k).view(np.float16)
+    for t, (_, want) in enumerate(cases):
+        assert np.all(y[t] == np.float16(want)), (t, y[t], want)
+    assert np.all(np.signbit(y[0]) == False)  # noqa: E712  (x + -x is +0 in round-to-nearest)
