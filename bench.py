@@ -6,10 +6,20 @@ input already resident in HBM: the dispatch tables built on the GPU from
 topk_ids (moe_build_dispatch), then phase 1 + phase 2 (moe_fused_forward).
 
 Metric: fused MoE forward TFLOP/s over valid rows, 2·pairs·3·hidden·intermediate
-per step ÷ step time.  Default workload: DeepSeek-V2-Lite-shaped (4096 tokens,
-top-6 of 64 experts, hidden 2048, intermediate 1408, uniform routing); its
-working set (1.45 GB) is far larger than the 129 MB L2, so back-to-back steps
-do not reuse L2 between iterations.
+per step ÷ step time, and the fraction of the roofline
+max(FLOPs / tensor peak, bytes / HBM peak).  Default workload: the largest one,
+DeepSeek-V3-shaped (16384 tokens, top-8 of 256 experts with Zipf(1.0)
+popularity, hidden 7168, intermediate 2048; 22.5 GB of expert weights).  Every
+non-tiny working set is far larger than the 129 MB L2, so back-to-back steps do
+not reuse L2 between iterations.
+
+Timing ("MetaX-TileLang工具链" §2.5: warm-up, then repeats; §2.5.2: mean,
+median, p90, p99, std): W warm-up steps (continued until --settle-s seconds of
+steps have run, so the power-capped clock has settled), then exactly K steps
+between synchronisations, timed with CUDA events on the launching stream.  A
+separate loop times steps one by one for the latency distribution, and another
+times the dispatch builder, phase 1 and phase 2 apart for the per-kernel
+rooflines.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead (the reference arm: the pages' own kernel targets a MetaX C500 and
@@ -25,6 +35,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -36,16 +47,24 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused MoE forward TFLOP/s (valid rows) and % of roofline on 1 GB300"
 UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "dsv3"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CPU_SAMPLE_EXPERTS = 8      # the oracle samples rows of at most this many experts (bounded host memory)
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=800)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--settle-s", type=float, default=3.0,
+                    help="warm-up continues until this many seconds of steps have run")
+    ap.add_argument("--phase-steps", type=int, default=500,
+                    help="steps of the per-kernel loop (outside the timed region)")
+    ap.add_argument("--latency-steps", type=int, default=200,
+                    help="steps timed one by one for the latency distribution")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="dsv2_lite")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample (cpu_baseline)")
@@ -53,11 +72,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step from Python instead of replaying a captured CUDA graph")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------
-# peaks, clocks, profiles
+# peaks, clocks, profiles, host
 # ---------------------------------------------------------------------------
 
 def load_peaks():
@@ -68,6 +87,25 @@ def load_peaks():
         return d, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 class ClockSampler:
@@ -121,7 +159,13 @@ class ClockSampler:
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         inside = [r for t, r in self.rows if self.t_begin and self.t_end and self.t_begin <= t <= self.t_end]
-        used = inside if inside else [r for _, r in self.rows]
+        used = inside
+        if len(used) < 3 and self.t_begin and self.t_end:
+            # a timed region shorter than a few sampling periods: take the
+            # last second of the (settled) warm-up as well
+            used = [r for t, r in self.rows if self.t_begin - 1.0 <= t <= self.t_end]
+        if not used:
+            used = [r for _, r in self.rows]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         sm, smax, pw = [], [], []
@@ -139,7 +183,8 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(used),
-                "samples_in_timed_region": len(inside)}
+                "samples_in_timed_region": len(inside),
+                "window": "timed region" if used is inside else "timed region and the second before it"}
 
 
 def kernel_source_hash():
@@ -157,10 +202,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per phase-1 launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"phase1_gate_up_{workload}.txt")
+def profile_traffic(workload: str, phase: int):
+    """DRAM bytes per launch of one GEMM phase from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    stem = "phase1_gate_up" if phase == 1 else "phase2_down"
+    path = os.path.join(ROOT, "profiles", f"{stem}_{workload}.txt")
     try:
         kv = {}
         with open(path) as f:
@@ -173,6 +219,79 @@ def profile_traffic(workload: str):
         return float(kv["dram_bytes_per_launch_full_size"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (host arithmetic on the group sizes)
+# ---------------------------------------------------------------------------
+
+def work_stats(w, sizes) -> dict:
+    """Algorithmic FLOPs and bytes per phase, and the padding statistics of the
+    grouped layout, from the workload's shape and its group sizes.
+
+    Bytes count every touched expert's weights once, every valid row's
+    activations once (x read, up_logits written and read back, out written,
+    routed weight read) and nothing for padding rows or re-reads.  Padding:
+    the allocated rows (num_blocks_m·128), the rows the page's "+1" rule pads
+    the groups to (Σ ceil((c+1)/128)·128) and the rows the kernels' 2-SM tiles
+    execute (each pair of an expert's active blocks and each lone active block
+    is one 256-row MMA tile)."""
+    import numpy as np
+    sizes = np.asarray(sizes, np.int64)
+    P, H, I, E = w.pairs, w.hidden, w.intermediate, w.experts
+    touched = int(np.count_nonzero(sizes))
+    active = -(-sizes // 128)
+    units = active // 2 + active % 2
+    m_blocks = -(-P // 128) + E
+    padded = int(np.sum(-(-(sizes + 1) // 128) * 128))
+    executed = int(256 * units.sum())
+    return {
+        "pairs": P, "touched_experts": touched, "active_blocks": int(active.sum()),
+        "tile_units": int(units.sum()), "alloc_rows": int(m_blocks * 128), "padded_rows": padded,
+        "padding_waste_rows": int(m_blocks * 128 - P), "padded_minus_valid_rows": padded - P,
+        "executed_mma_rows": executed, "executed_row_ratio": executed / P if P else 0.0,
+        "flops": 6.0 * P * H * I, "flops_phase1": 4.0 * P * H * I, "flops_phase2": 2.0 * P * H * I,
+        "weight_bytes": 6.0 * H * I * touched,
+        "weight_bytes_phase1": 4.0 * H * I * touched, "weight_bytes_phase2": 2.0 * H * I * touched,
+        "activation_bytes": P * (2.0 * H + 2.0 * H + 4.0 + 4.0 * I),
+        "activation_bytes_no_up_logits": P * (2.0 * H + 2.0 * H + 4.0),
+        "activation_bytes_phase1": P * (2.0 * H + 2.0 * I),
+        "activation_bytes_phase2": P * (2.0 * I + 2.0 * H + 4.0),
+    }
+
+
+def touched_bytes(w, sizes):
+    """(touched-expert weight bytes, activation bytes, touched experts)."""
+    s = work_stats(w, sizes)
+    return s["weight_bytes"], s["activation_bytes"], s["touched_experts"]
+
+
+def kernel_roofline(name, flops, nbytes, ms, tc_peak, hbm_peak, tc_label, traffic=None, extra=None):
+    """Roofline of one kernel: bound = whichever of FLOP time and byte time is
+    larger; achieved in that resource's unit ÷ its peak."""
+    t_flop = flops / (tc_peak * 1e12)
+    t_byte = nbytes / (hbm_peak * 1e9)
+    if t_flop >= t_byte:
+        r = {"kernel": name, "bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": tc_peak,
+             "unit": "TFLOP/s"}
+    else:
+        r = {"kernel": name, "bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm_peak,
+             "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r.update({"traffic": traffic, "launch_ms": ms, "algorithmic_flops_per_launch": flops,
+              "algorithmic_bytes_per_launch": nbytes, "t_flop_ms": 1e3 * t_flop, "t_byte_ms": 1e3 * t_byte,
+              "tensor_peak_kind": tc_label})
+    if extra:
+        r.update(extra)
+    return r
+
+
+def latency_stats(ms_list):
+    import numpy as np
+    a = np.asarray(ms_list, np.float64)
+    return {"n": int(a.size), "mean": float(a.mean()), "median": float(np.median(a)),
+            "p90": float(np.percentile(a, 90)), "p99": float(np.percentile(a, 99)),
+            "std": float(a.std(ddof=1)) if a.size > 1 else 0.0, "min": float(a.min()), "max": float(a.max())}
 
 
 # ---------------------------------------------------------------------------
@@ -189,7 +308,6 @@ def prepare_device(w, seed, dev):
     ids_np, tw_np = workloads.routing(w, seed)
     x_np = workloads.tokens(w, seed)
     gate, up, down = workloads.expert_weights(w, seed, device=str(dev))
-    T, k = ids_np.shape
     ids = torch.from_numpy(ids_np).to(dev)
     tables = moe.build_dispatch(ids, w.experts)
     rows_total = tables["group_idx_for_bx"].numel() * moe.BLOCK_TOKEN
@@ -205,90 +323,136 @@ def prepare_device(w, seed, dev):
                 x_tok=x_tok, tw=tw)
 
 
-def touched_bytes(w, sizes):
-    import numpy as np
-    touched = int(np.count_nonzero(sizes))
-    wbytes = 6.0 * w.hidden * w.intermediate * touched
-    P = w.pairs
-    act = P * (2.0 * w.hidden + 2.0 * w.hidden + 4.0 + 4.0 * w.intermediate)
-    return wbytes, act, touched
-
-
 # ---------------------------------------------------------------------------
 # oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(w, seed, target_s, host=None):
-    """Time the CPU oracle on a bounded sample of valid rows of the workload.
-    Returns (TFLOP/s, sample description, threads, seconds)."""
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: valid rows of at
+    most CPU_SAMPLE_EXPERTS experts, with host copies of those experts'
+    weights only (the other experts' slices are never read and stay
+    unallocated zero pages).  Every valid row costs the oracle the same
+    6·H·I FLOPs whatever its expert, so the rate is that of the workload."""
+
+    def __init__(self, w, seed, weights_of, experts_from_front=False):
+        import numpy as np
+
+        import oracle
+        import workloads
+        self.w = w
+        ids_np, tw_np = workloads.routing(w, seed)
+        x_np = workloads.tokens(w, seed)
+        self.tab = oracle.build_dispatch(ids_np, w.experts)
+        prow = oracle.pair_padded_rows(ids_np, w.experts, self.tab["group_padded_offsets"])
+        rows_total = self.tab["num_blocks_m"] * oracle.BLOCK_TOKEN
+        self.xo, self.rwo = oracle.pack(x_np, ids_np, tw_np, prow, self.tab, rows_total)
+        sizes = self.tab["group_sizes"]
+        nonempty = np.nonzero(sizes)[0]
+        rng = np.random.default_rng(seed + 17)
+        n_e = min(CPU_SAMPLE_EXPERTS, nonempty.size)
+        if experts_from_front:
+            chosen = nonempty[:n_e]
+        else:
+            chosen = np.sort(rng.choice(nonempty, size=n_e, replace=False))
+        self.how = "first non-empty" if experts_from_front else "randomly chosen"
+        self.experts = [int(e) for e in chosen]
+        E, I, H = w.experts, w.intermediate, w.hidden
+        self.g = np.zeros((E, I, H), np.float16)
+        self.u = np.zeros((E, I, H), np.float16)
+        self.d = np.zeros((E, H, I), np.float16)
+        for e, (ge, ue, de) in zip(self.experts, weights_of(self.experts)):
+            self.g[e], self.u[e], self.d[e] = ge, ue, de
+        ex = np.zeros(E, bool)
+        ex[self.experts] = True
+        flat = prow.reshape(-1)
+        self.valid = flat[ex[ids_np.reshape(-1)]]
+        self.n_valid_total = flat.size
+        self.threads = len(os.sched_getaffinity(0))
+        self.rng = np.random.default_rng(seed)
+        self.per_row_flops = 6.0 * H * I
+
+    def run(self, n, n_threads=None):
+        import oracle
+        rows = self.rng.choice(self.valid, size=min(n, self.valid.size), replace=False)
+        t0 = time.perf_counter()
+        oracle.forward_rows(self.xo, self.g, self.u, self.d, self.rwo, self.tab, rows,
+                            n_threads=self.threads if n_threads is None else n_threads)
+        return rows.size, time.perf_counter() - t0
+
+    def describe(self, n):
+        return (f"{n} randomly chosen valid rows (of the {self.valid.size} rows of {len(self.experts)} "
+                f"{self.how} experts; {self.n_valid_total} valid rows in all), each row's full "
+                f"phase 1 and phase 2 with fp32 accumulation, {self.threads} OpenMP threads")
+
+    def rate(self, target_s):
+        """(TFLOP/s, rows, seconds) of a sample sized to take about target_s."""
+        n0 = min(self.valid.size, max(self.threads, 8))
+        _, t0 = self.run(n0)
+        n = int(min(self.valid.size, max(n0, round(n0 * target_s / max(t0, 1e-6)))))
+        n, dt = self.run(n)
+        return n * self.per_row_flops / dt / 1e12, n, dt
+
+
+def tiny_single_thread():
+    """The oracle's whole forward on the tiny workload with one thread:
+    (TFLOP/s, seconds per forward, best of 3)."""
     import numpy as np
 
     import oracle
     import workloads
-
-    if host is None:
-        ids_np, tw_np = workloads.routing(w, seed)
-        x_np = workloads.tokens(w, seed)
-        g, u, d = workloads.expert_weights(w, seed, device="cpu")
-        host = dict(ids_np=ids_np, tw_np=tw_np, x_np=x_np, g=g.numpy(), u=u.numpy(), d=d.numpy())
-    tab = oracle.build_dispatch(host["ids_np"], w.experts)
-    prow = oracle.pair_padded_rows(host["ids_np"], w.experts, tab["group_padded_offsets"])
-    rows_total = tab["num_blocks_m"] * oracle.BLOCK_TOKEN
-    xo, rwo = oracle.pack(host["x_np"], host["ids_np"], host["tw_np"], prow, tab, rows_total)
-    threads = len(os.sched_getaffinity(0))
-    rng = np.random.default_rng(seed)
-    valid = prow.reshape(-1)
-    per_row_flops = 6.0 * w.hidden * w.intermediate
-
-    def run(n):
-        rows = rng.choice(valid, size=n, replace=False)
+    w = workloads.WORKLOADS["tiny"]
+    ids, tw = workloads.routing(w, 0)
+    x = workloads.tokens(w, 0)
+    g, u, d = (t.numpy() for t in workloads.expert_weights(w, 0, device="cpu"))
+    tab = oracle.build_dispatch(ids, w.experts)
+    prow = oracle.pair_padded_rows(ids, w.experts, tab["group_padded_offsets"])
+    xo, rwo = oracle.pack(x, ids, tw, prow, tab, tab["num_blocks_m"] * oracle.BLOCK_TOKEN)
+    best = np.inf
+    for _ in range(3):
         t0 = time.perf_counter()
-        oracle.forward_rows(xo, host["g"], host["u"], host["d"], rwo, tab, rows, n_threads=threads)
-        return time.perf_counter() - t0
+        oracle.fused_forward(xo, g, u, d, rwo, tab, n_threads=1)
+        best = min(best, time.perf_counter() - t0)
+    return w.flops() / best / 1e12, best
 
-    n0 = min(valid.size, max(threads, 8))
-    t0 = run(n0)
-    n = int(min(valid.size, max(n0, round(n0 * target_s / max(t0, 1e-6)))))
-    dt = run(n)
-    rate = n * per_row_flops / dt / 1e12
-    desc = (f"{n} randomly chosen valid rows of {valid.size} (each row's full phase 1 and "
-            f"phase 2, fp32 accumulation), {threads} OpenMP threads")
-    return rate, desc, threads, dt, host, (xo, rwo, tab, valid)
+
+def _cpu_weights_front(w, seed):
+    """Weights for the reference arm, drawn on the host for the first experts only."""
+    import workloads
+
+    def weights_of(experts):
+        n = max(experts) + 1
+        g, u, d = workloads.expert_weights(w, seed, device="cpu", experts=n)
+        return [(g[e].numpy(), u[e].numpy(), d[e].numpy()) for e in experts]
+    return weights_of
 
 
 def reference_arm(args, w):
-    import numpy as np
-
-    import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     # size each step so that warmup + steps finish within ~3 minutes
     budget = 180.0 / max(1, args.steps + args.warmup)
     per_step_target = max(0.2, min(3.0, budget))
-    rate0, _, threads, _, host, (xo, rwo, tab, valid) = oracle_sample_rate(w, args.seed, per_step_target)
-    per_row = 6.0 * w.hidden * w.intermediate
-    n = max(1, int(rate0 * 1e12 * per_step_target / per_row))
-    n = min(n, valid.size)
-    rng = np.random.default_rng(args.seed + 1)
+    smp = OracleSample(w, args.seed, _cpu_weights_front(w, args.seed), experts_from_front=True)
+    rate0, _, _ = smp.rate(per_step_target)
+    n = max(1, int(rate0 * 1e12 * per_step_target / smp.per_row_flops))
+    n = min(n, smp.valid.size)
     times = []
     for i in range(args.warmup + args.steps):
-        rows = rng.choice(valid, size=n, replace=False)
-        t0 = time.perf_counter()
-        oracle.forward_rows(xo, host["g"], host["u"], host["d"], rwo, tab, rows, n_threads=threads)
+        n_done, dt = smp.run(n)
         if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
+            times.append(dt)
     ms = 1e3 * sum(times) / len(times)
-    value = n * per_row / (ms / 1e3) / 1e12
-    sample = (f"per step {n} randomly chosen valid rows of {valid.size} (each row's full phase 1 "
-              f"and phase 2), {threads} OpenMP threads")
+    value = n_done * smp.per_row_flops / (ms / 1e3) / 1e12
+    sample = "per step " + smp.describe(n_done)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_of(w, "host cores; bounded sample per step"),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "latency_ms": latency_stats([1e3 * t for t in times]),
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
@@ -320,8 +484,8 @@ def config_of(w, l2):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def main():
-    args = parse_args()
+def main(argv=None):
+    args = parse_args(argv)
     import workloads
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -368,12 +532,14 @@ def main():
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     run_step = step
+    run_one = step
     per_replay = 1          # steps per launch of run_step
     if not args.eager:
         # S consecutive steps (each: dispatch tables, phase 1, phase 2 with its
         # programmatic dependency) captured as one CUDA graph, replayed
         # steps / S times; S = 8 when it divides the step count, which spreads
-        # the graph-launch gap (~3 us) over 8 steps
+        # the graph-launch gap (~3 us) over 8 steps.  A one-step graph serves
+        # the latency loop.
         per_replay = 8 if args.steps % 8 == 0 else 1
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
@@ -386,10 +552,23 @@ def main():
             for _ in range(per_replay):
                 step()
         run_step = graph.replay
-    warm_launches = -(-max(3, args.warmup) // per_replay)
-    warmup_steps = warm_launches * per_replay
-    for _ in range(warm_launches):
+        graph1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph1):
+            step()
+        run_one = graph1.replay
+
+    # warm-up: at least W steps (and 3), continued until settle_s seconds of
+    # steps have run so that the timed region sees the settled clock
+    warm_launches = 0
+    t_settle = time.perf_counter()
+    while True:
         run_step()
+        warm_launches += 1
+        if warm_launches * per_replay >= max(3, args.warmup):
+            torch.cuda.synchronize(dev)
+            if time.perf_counter() - t_settle >= args.settle_s:
+                break
+    warmup_steps = warm_launches * per_replay
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
@@ -408,10 +587,20 @@ def main():
     flops = w.flops()
     value = job_value(world, flops, ms)
 
-    # ---- per-phase durations (same stream, CUDA events) -------------------
-    # (enough steps that the power-capped clock settles as in the timed loop;
-    # the second half is averaged)
-    n_ph = max(6, min(args.steps, 500))
+    # ---- latency distribution: steps timed one by one ----------------------
+    n_lat = max(10, args.latency_steps)
+    lat_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_lat)]
+    for a_, b_ in lat_ev:
+        a_.record()
+        run_one()
+        b_.record()
+    torch.cuda.synchronize(dev)
+    latency = latency_stats([a_.elapsed_time(b_) for a_, b_ in lat_ev])
+
+    # ---- per-kernel durations (same stream, CUDA events) -------------------
+    # a fixed number of steps whatever --steps is, so the power-capped clock
+    # settles as in the timed loop; the second half is averaged
+    n_ph = max(6, args.phase_steps)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ph)]
     for i in range(n_ph):
         e = evs[i]
@@ -441,6 +630,7 @@ def main():
     # computes, and its D2H on a third stream while step i+1 computes.  The
     # serial form (everything on one stream) is timed too.
     e2e = None
+    pack_ms = combine_ms = None
     if not args.no_e2e:
         h_ids = d["ids"].cpu().pin_memory()
         h_x = d["x_tok"].cpu().pin_memory()
@@ -464,10 +654,13 @@ def main():
         for e_ in ev_used + ev_out:
             e_.record(comp)
 
-        def compute(ids_, x_, tw_, y_):
-            moe.build_dispatch(ids_, E, out=t)
+        def pack(ids_, x_, tw_):
             moe.pack_routed(ids_, tw_, x_, t, d["rows_total"], stacked=d["xp"], routed_weights=d["rw"],
                             pair_rows=prows, workspace=ws)
+
+        def compute(ids_, x_, tw_, y_):
+            moe.build_dispatch(ids_, E, out=t)
+            pack(ids_, x_, tw_)
             return lambda: (moe.fused_forward(d["xp"], d["gate"], d["up"], d["down"], d["rw"],
                                               t["group_sizes"], t["group_offsets"], t["group_padded_offsets"],
                                               t["group_idx_for_bx"], d["ul"], d["out"]),
@@ -534,13 +727,27 @@ def main():
                        "copies on two side streams with double-buffered staging, overlapping the "
                        "neighbouring steps' compute"}
 
+        # pack (three launches) and combine timed apart, same stream, events
+        n_pc = 50
+        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_pc)]
+        for e in pev:
+            e[0].record()
+            pack(d["ids"], d["x_tok"], d["tw"])
+            e[1].record()
+            moe.combine_routed(d["out"], prows, y=d_y[0])
+            e[2].record()
+        torch.cuda.synchronize(dev)
+        pack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in pev[n_pc // 2:])
+        combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in pev[n_pc // 2:])
+
     # ---- timing scopes of the evaluation page: the whole MoE layer ---------
     # cached_e2e: router -> dispatch -> pack -> forward -> combine on tokens
     # already on the device, all buffers reused (routing from a random router,
     # so it is near-uniform whatever the workload's own routing is);
     # e2e_host: the same with the tokens copied in and the outputs copied out.
     scopes = None
-    if not args.no_e2e:
+    router_ms = None
+    if not args.no_e2e and E <= moe.ROUTER_MAX_EXPERTS:
         wg = torch.from_numpy(workloads.router_weights(w, args.seed + rank)).to(dev)
         ids_l = torch.empty_like(d["ids"])
         tw_l = torch.empty_like(d["tw"])
@@ -584,6 +791,7 @@ def main():
         n_sc = max(5, min(args.steps, 100))
         cached_ms = max_over_ranks(time_fn(lambda: layer(x_l), n_sc), dist, dev)
         host_ms = max_over_ranks(time_fn(layer_host, n_sc), dist, dev)
+        router_ms = time_fn(lambda: moe.router_topk(x_l, wg, w.top_k, topk_ids=ids_l, topk_weights=tw_l), 50)
         router_flops = 2.0 * w.tokens * w.hidden * w.experts
         scopes = {"routed_kernel_only_ms": ms, "cached_e2e_ms": cached_ms, "e2e_host_ms": host_ms,
                   "cached_e2e_tflops": job_value(world, flops + router_flops, cached_ms),
@@ -592,42 +800,76 @@ def main():
                                 "router (near-uniform), not the workload's own routing",
                   "launches_per_layer": 8}
 
-    # ---- roofline --------------------------------------------------------------
+    # ---- rooflines ---------------------------------------------------------------
     peaks, src = load_peaks()
-    sizes = t["group_sizes"].cpu().numpy()
-    wbytes, act, touched = touched_bytes(w, sizes)
-    p1_flops = 4.0 * w.pairs * w.hidden * w.intermediate
-    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    ws_ = work_stats(w, t["group_sizes"].cpu().numpy())
+    tc_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tc_sust = float(peaks.get("bf16_tflops_sustained", tc_burst))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    achieved = p1_flops / (p1_ms * 1e-3) / 1e12
-    traffic = profile_traffic(w.name)
-    tc_sust = float(peaks.get("bf16_tflops_sustained", tc_peak))
-    roof = {"kernel": "grouped_gemm_kernel<1> (phase 1: gate+up GEMM, SiLU·up epilogue)",
-            "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-            "frac": achieved / tc_peak, "traffic": traffic,
-            "peak_source": f"{src} bf16 dense burst (fp16 dense rate is the same on this part)",
-            "frac_vs_sustained_peak": achieved / tc_sust, "sustained_peak": tc_sust,
-            "algorithmic_flops_per_launch": p1_flops, "launch_ms": p1_ms}
-    fwd_ms = p1_ms + p2_ms
-    t_flop = flops / (tc_peak * 1e12)
-    t_byte = (wbytes + act) / (hbm * 1e9)
-    forward_roofline = {"t_roof_ms": 1e3 * max(t_flop, t_byte), "t_flop_ms": 1e3 * t_flop,
-                        "t_byte_ms": 1e3 * t_byte, "bound": "tensor" if t_flop >= t_byte else "hbm",
-                        "touched_weight_bytes": wbytes, "activation_bytes": act,
-                        "touched_experts": touched, "phase1_ms": p1_ms, "phase2_ms": p2_ms,
-                        "dispatch_ms": dispatch_ms, "step_ms": ms,
-                        "frac_of_step": 1e3 * max(t_flop, t_byte) / ms,
-                        "frac_of_step_vs_sustained_peak": 1e3 * max(flops / (tc_sust * 1e12), t_byte) / ms,
-                        "peaks": f"{src}: {tc_peak} TFLOP/s burst, {tc_sust} TFLOP/s sustained "
-                                 f"(power-capped back-to-back GEMMs), {hbm} GB/s"}
+    # the per-kernel loop runs hundreds of back-to-back steps under the power
+    # cap, so its kernels are held against the sustained dense peak (the burst
+    # fraction is given beside it)
+    tc_label = f"{src} bf16 dense sustained (fp16 dense rate is the same on this part)"
+    H, I = w.hidden, w.intermediate
+    k1 = kernel_roofline("grouped_gemm_kernel<1> (phase 1: gate+up GEMM, SiLU·up epilogue)",
+                         ws_["flops_phase1"], ws_["weight_bytes_phase1"] + ws_["activation_bytes_phase1"],
+                         p1_ms, tc_sust, hbm, tc_label, traffic=profile_traffic(w.name, 1))
+    k2 = kernel_roofline("grouped_gemm_kernel<2> (phase 2: down GEMM, routed-weight epilogue)",
+                         ws_["flops_phase2"], ws_["weight_bytes_phase2"] + ws_["activation_bytes_phase2"],
+                         p2_ms, tc_sust, hbm, tc_label, traffic=profile_traffic(w.name, 2))
+    for k in (k1, k2):
+        if k["bound"] == "tensor":
+            k["frac_vs_burst_peak"] = k["achieved"] / tc_burst
+            k["burst_peak"] = tc_burst
+    kd = kernel_roofline("build_dispatch_kernel", 0.0, 4.0 * w.pairs + 4.0 * (3 * E + 2 + ws_["alloc_rows"] // 128),
+                         dispatch_ms, tc_sust, hbm, tc_label)
+    kernels = [k1, k2, kd]
+    if pack_ms is not None:
+        kernels.append(kernel_roofline(
+            "pack (rank_chunks_kernel + scan_chunks_kernel + place_pairs_kernel)", 0.0,
+            w.pairs * (2.0 * H + 2.0 * H + 4 + 4 + 4 + 4) + 4.0 * w.pairs, pack_ms, tc_sust, hbm, tc_label,
+            extra={"bytes_note": "per pair: token row read 2H + packed row written 2H + id, weight, "
+                                 "compact weight, padded row; ids read once more for the ranks"}))
+        kernels.append(kernel_roofline(
+            "combine_kernel", 0.0, w.pairs * (2.0 * H + 4) + w.tokens * 2.0 * H, combine_ms, tc_sust, hbm,
+            tc_label, extra={"bytes_note": "per pair: expert row read 2H + its padded row 4; per token: "
+                                           "output row written 2H"}))
+    if router_ms is not None:
+        kernels.append(kernel_roofline(
+            "router_kernel", 2.0 * w.tokens * H * E, 2.0 * w.tokens * H + 2.0 * E * H + 8.0 * w.pairs,
+            router_ms, tc_sust, hbm, tc_label))
+    roof = max((k1, k2), key=lambda k: k["launch_ms"])     # the dominant kernel of the step
+
+    t_flop = ws_["flops"] / (tc_burst * 1e12)
+    t_flop_s = ws_["flops"] / (tc_sust * 1e12)
+    t_byte = (ws_["weight_bytes"] + ws_["activation_bytes"]) / (hbm * 1e9)
+    t_byte_nul = (ws_["weight_bytes"] + ws_["activation_bytes_no_up_logits"]) / (hbm * 1e9)
+    forward_roofline = {
+        "t_roof_ms": 1e3 * max(t_flop, t_byte), "t_flop_ms": 1e3 * t_flop, "t_byte_ms": 1e3 * t_byte,
+        "t_byte_ms_without_up_logits": 1e3 * t_byte_nul,
+        "bound": "tensor" if t_flop >= t_byte else "hbm",
+        "frac_of_step": 1e3 * max(t_flop, t_byte) / ms,
+        "frac_of_step_vs_sustained_peak": 1e3 * max(t_flop_s, t_byte) / ms,
+        "phase1_ms": p1_ms, "phase2_ms": p2_ms, "dispatch_ms": dispatch_ms, "step_ms": ms,
+        "peaks": f"{src}: {tc_burst} TFLOP/s burst, {tc_sust} TFLOP/s sustained "
+                 f"(power-capped back-to-back GEMMs), {hbm} GB/s"}
+    work = {k: ws_[k] for k in ("pairs", "touched_experts", "active_blocks", "tile_units", "alloc_rows",
+                                "padded_rows", "padding_waste_rows", "padded_minus_valid_rows",
+                                "executed_mma_rows", "executed_row_ratio", "weight_bytes", "activation_bytes",
+                                "activation_bytes_no_up_logits")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = dict(ids_np=d["ids_np"], tw_np=d["tw_np"], x_np=d["x_np"], g=d["gate"].cpu().numpy(),
-                    u=d["up"].cpu().numpy(), d=d["down"].cpu().numpy())
-        rate, desc, threads, secs, _, _ = oracle_sample_rate(w, args.seed, args.cpu_seconds, host=host)
-        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
-               "seconds": secs}
+        def weights_of(experts):
+            return [(d["gate"][e].cpu().numpy(), d["up"][e].cpu().numpy(), d["down"][e].cpu().numpy())
+                    for e in experts]
+        smp = OracleSample(w, args.seed, weights_of)
+        rate, n, secs = smp.rate(args.cpu_seconds)
+        tiny_rate, tiny_s = tiny_single_thread()
+        cpu = {"value": rate, "unit": UNIT, "cores": smp.threads, "kind": "oracle", "sample": smp.describe(n),
+               "seconds": secs, "cpu_model": cpu_model(),
+               "tiny_single_thread": {"value": tiny_rate, "unit": UNIT, "seconds_per_forward": tiny_s,
+                                      "threads": 1, "sample": "the whole tiny forward (128 valid rows)"}}
 
     if rank == 0:
         clocks = sampler.summary()
@@ -636,11 +878,14 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
                 "config": config_of(w, "working set larger than L2 (no flush needed)"),
                 "parallelism": "replicas only" if world > 1 else "single GPU",
-                "roofline": roof, "forward_roofline": forward_roofline,
+                "roofline": roof, "forward_roofline": forward_roofline, "kernels": kernels,
+                "latency_ms": latency, "work": work,
                 "cpu_baseline": cpu, "e2e": e2e, "scopes": scopes, "clocks": clocks,
                 "gpu_launches": 3 * args.steps, "device_status": dev_status,
                 "launch_mode": "eager" if args.eager else
                 f"cuda_graph ({per_replay} step(s) captured per graph, replayed steps/{per_replay} times)",
+                "warmup_note": f"at least {max(3, args.warmup)} warm-up steps, continued for "
+                               f"{args.settle_s:g} s so the timed region runs at the settled clock",
                 "kernel_source_sha": kernel_source_hash()}
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -42,3 +42,48 @@ def test_decode_touches_a_subset_of_experts():
     assert touched == int(np.count_nonzero(sizes)) and 40 < touched < w.experts
     assert wbytes == 6.0 * w.hidden * w.intermediate * touched
     assert act == pytest.approx(2.9e6, rel=5e-2)
+
+
+def test_default_workload_is_the_largest():
+    args = bench.parse_args([])
+    assert args.workload == "dsv3"
+    big = max(workloads.WORKLOADS.values(), key=lambda w: w.flops())
+    assert big.name == args.workload
+
+
+def test_padding_statistics_by_hand():
+    """Three experts with 0, 128 and 300 rows: the "+1" rule pads them to 128,
+    256 and 384 rows; their active blocks are 0, 1 and 3; the 2-SM tiles are
+    0, 1 (a lone block) and 2 (a pair plus a lone block), 256 rows each."""
+    w = workloads.Workload("hand", 107, 4, 3, 256, 512)
+    assert w.pairs == 428
+    s = bench.work_stats(w, np.array([0, 128, 300]))
+    assert s["padded_rows"] == 128 + 256 + 384
+    assert s["active_blocks"] == 4 and s["tile_units"] == 3
+    assert s["executed_mma_rows"] == 3 * 256
+    assert s["alloc_rows"] == (4 + 3) * 128
+    assert s["padding_waste_rows"] == 7 * 128 - 428
+    assert s["padded_minus_valid_rows"] == 768 - 428
+    assert s["touched_experts"] == 2
+    assert s["flops_phase1"] + s["flops_phase2"] == w.flops()
+    assert s["activation_bytes"] == s["activation_bytes_phase1"] + s["activation_bytes_phase2"]
+    assert s["activation_bytes"] - s["activation_bytes_no_up_logits"] == 428 * 4 * 512
+
+
+@pytest.mark.parametrize("name,bound1", [("dsv3", "tensor"), ("mixtral", "tensor"), ("decode_skewed", "hbm")])
+def test_kernel_bound_follows_its_own_times(name, bound1):
+    """Phase 1's bound is the larger of its FLOP time and byte time at the
+    peaks: the compute-heavy shapes are tensor-bound, the decode shape (a few
+    rows per expert, every touched expert's weights streamed once) HBM-bound,
+    and the fraction is then reported in GB/s against the HBM peak."""
+    w = workloads.WORKLOADS[name]
+    ids, _ = workloads.routing(w, 0)
+    s = bench.work_stats(w, oracle.build_dispatch(ids, w.experts)["group_sizes"])
+    r = bench.kernel_roofline("p1", s["flops_phase1"], s["weight_bytes_phase1"] + s["activation_bytes_phase1"],
+                              1.0, 1700.0, 6700.0, "test")
+    assert r["bound"] == bound1
+    if bound1 == "hbm":
+        assert r["unit"] == "GB/s" and r["achieved"] == pytest.approx(r["algorithmic_bytes_per_launch"] / 1e6)
+    else:
+        assert r["unit"] == "TFLOP/s" and r["achieved"] == pytest.approx(s["flops_phase1"] / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
