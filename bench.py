@@ -234,8 +234,8 @@ def work_stats(w, sizes) -> dict:
     routed weight read) and nothing for padding rows or re-reads.  Padding:
     the allocated rows (num_blocks_m·128), the rows the page's "+1" rule pads
     the groups to (Σ ceil((c+1)/128)·128) and the rows the kernels' 2-SM tiles
-    execute (each pair of an expert's active blocks and each lone active block
-    is one 256-row MMA tile)."""
+    execute (each pair of an expert's active blocks is one 256-row MMA tile,
+    each lone active block one 128-row tile)."""
     import numpy as np
     sizes = np.asarray(sizes, np.int64)
     P, H, I, E = w.pairs, w.hidden, w.intermediate, w.experts
@@ -244,7 +244,7 @@ def work_stats(w, sizes) -> dict:
     units = active // 2 + active % 2
     m_blocks = -(-P // 128) + E
     padded = int(np.sum(-(-(sizes + 1) // 128) * 128))
-    executed = int(256 * units.sum())
+    executed = int(256 * (active // 2).sum() + 128 * (active % 2).sum())
     return {
         "pairs": P, "touched_experts": touched, "active_blocks": int(active.sum()),
         "tile_units": int(units.sum()), "alloc_rows": int(m_blocks * 128), "padded_rows": padded,
@@ -827,9 +827,10 @@ def main(argv=None):
     if pack_ms is not None:
         kernels.append(kernel_roofline(
             "pack (rank_chunks_kernel + scan_chunks_kernel + place_pairs_kernel)", 0.0,
-            w.pairs * (2.0 * H + 2.0 * H + 4 + 4 + 4 + 4) + 4.0 * w.pairs, pack_ms, tc_sust, hbm, tc_label,
-            extra={"bytes_note": "per pair: token row read 2H + packed row written 2H + id, weight, "
-                                 "compact weight, padded row; ids read once more for the ranks"}))
+            w.tokens * 2.0 * H + w.pairs * (2.0 * H + 4 + 4 + 4 + 4) + 4.0 * w.pairs, pack_ms, tc_sust, hbm,
+            tc_label,
+            extra={"bytes_note": "per token: its row read once 2H; per pair: packed row written 2H + id, "
+                                 "weight, compact weight, padded row; ids read once more for the ranks"}))
         kernels.append(kernel_roofline(
             "combine_kernel", 0.0, w.pairs * (2.0 * H + 4) + w.tokens * 2.0 * H, combine_ms, tc_sust, hbm,
             tc_label, extra={"bytes_note": "per pair: expert row read 2H + its padded row 4; per token: "

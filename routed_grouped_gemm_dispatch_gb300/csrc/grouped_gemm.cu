@@ -22,8 +22,13 @@
 //    CTA's shared memory holds only half of the weight tile (128 of its 256
 //    rows) and the pair shares it.  Per SM this halves the weight bytes that
 //    TMA writes into and the tensor core reads out of shared memory, which is
-//    what limits a one-SM 128 x 256 tile.  A single block runs the same tile
-//    with zero rows in the odd CTA, whose results are not stored.
+//    what limits a one-SM 128 x 256 tile.  A SINGLE block runs as a 2-SM tile
+//    with M = 128: each CTA holds 64 of the block's rows, so no MMA work goes
+//    to a second, empty block.  The M = 128 accumulator of a CTA sits in 128
+//    TMEM columns: lanes 0-63 hold its rows' columns 0-127 of N, lanes 64-127
+//    the same rows' columns 128-255.  In phase 1 each CTA's half of B is then
+//    64 gate rows followed by the same 64 up rows, so a thread finds the gate
+//    and up values of its outputs in its own lane.
 //  * Tiles are ordered in groups of about one expert's units, slice by slice
 //    inside a group (see decode_tile), so concurrent clusters share each
 //    weight slice in L2 instead of re-reading it once per unit.
@@ -73,6 +78,10 @@ constexpr int SMALL_ROWS = 32;                // blocks with at most this many r
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s per drain wait
 constexpr uint32_t IDESC = idesc_f16_f32acc(2 * BM, BN);   // M = 256 across the pair
+constexpr uint32_t IDESC_M128 = idesc_f16_f32acc(BM, BN);  // M = 128 across the pair (a lone block)
+constexpr int HALF_ROWS = BM / 2;                          // rows of a lone block each CTA holds
+constexpr uint32_t A16_BYTES = A_BOX_BYTES / 8;            // a 16-row box of A
+constexpr uint32_t A64_BYTES = A_BOX_BYTES / 2;            // a 64-row box of A
 constexpr int64_t GROUP_A_BYTES = 32ll << 20;     // A rows a tile-order group keeps hot in L2
 constexpr int32_t UNITS_PER_EXPERT_MULT = 1;
 
@@ -158,10 +167,9 @@ __device__ __forceinline__ int32_t block_rows(const GemmParams& p, int32_t bx, i
 struct Tile {
     int32_t u;        // unit
     int32_t bx0;      // first block of the unit (the expert comes from it)
-    int32_t bx;       // block whose rows this CTA holds
+    int32_t bx;       // block whose rows this CTA holds (a lone block: both CTAs hold half of it)
     int32_t n;        // N slice
-    bool pair;
-    bool store;       // false: the odd CTA of a single block (its rows are discarded)
+    bool pair;        // true: M = 256 over two blocks; false: M = 128 over one block
 };
 
 __device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, int32_t n_tiles,
@@ -178,7 +186,6 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, in
     ti.bx0 = units[u] & 0x7FFF;
     ti.pair = (units[u] & PAIR_BIT) != 0;
     ti.bx = ti.pair ? ti.bx0 + static_cast<int32_t>(rank) : ti.bx0;
-    ti.store = ti.pair || rank == 0;
     return ti;
 }
 
@@ -271,17 +278,22 @@ __device__ __forceinline__ bool counter_wait_bounded(const int32_t* counter, int
     }
 }
 
-// map_x / map_x16: x (boxes 64 x 128 and 64 x 16 rows); map_gate / map_up:
-// phase-1 weights (box 64 x 128); map_u / map_u16: up_logits; map_down:
-// phase-2 weights (box 64 x 128).  A launch of one phase gets placeholders for
-// the other phase's maps.
+// map_x / map_x64 / map_x16: x (boxes of 128, 64 and 16 rows, 64 wide);
+// map_gate / map_up: phase-1 weights (boxes of 128 rows), map_gate64 /
+// map_up64 (64 rows, for M = 128 tiles); map_u / map_u64 / map_u16:
+// up_logits; map_down: phase-2 weights (128 rows).  A launch of one phase gets
+// placeholders for the other phase's maps.
 template <int PHASE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
+                    const __grid_constant__ CUtensorMap map_x64,
                     const __grid_constant__ CUtensorMap map_x16,
                     const __grid_constant__ CUtensorMap map_gate,
                     const __grid_constant__ CUtensorMap map_up,
+                    const __grid_constant__ CUtensorMap map_gate64,
+                    const __grid_constant__ CUtensorMap map_up64,
                     const __grid_constant__ CUtensorMap map_u,
+                    const __grid_constant__ CUtensorMap map_u64,
                     const __grid_constant__ CUtensorMap map_u16,
                     const __grid_constant__ CUtensorMap map_down,
                     const GemmParams p) {
@@ -325,12 +337,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     if (warp == 0 && lane == 0) {
         if (PHASE != 2) {
             tma_prefetch_map(&map_x);
+            tma_prefetch_map(&map_x64);
             tma_prefetch_map(&map_x16);
             tma_prefetch_map(&map_gate);
             tma_prefetch_map(&map_up);
+            tma_prefetch_map(&map_gate64);
+            tma_prefetch_map(&map_up64);
         }
         if (PHASE != 1) {
             tma_prefetch_map(&map_u);
+            tma_prefetch_map(&map_u64);
             tma_prefetch_map(&map_u16);
             tma_prefetch_map(&map_down);
         }
@@ -470,14 +486,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                                       : ti.n * BN + static_cast<int32_t>(rank) * 128 < p.ph[1].n_extent,
                            p.status);
                 const CUtensorMap* a_map = pt.ph == 1 ? &map_x : &map_u;
+                const CUtensorMap* a64_map = pt.ph == 1 ? &map_x64 : &map_u64;
                 const CUtensorMap* a16_map = pt.ph == 1 ? &map_x16 : &map_u16;
                 if (PHASE == 3 && pt.ph == 2) {
                     // this tile reads the unit's up_logits rows: wait until every
-                    // phase-1 tile of the unit has stored them (both CTAs for a
-                    // pair, the even CTA for a single), then order those generic
-                    // stores before this thread's TMA (async proxy) reads
+                    // phase-1 tile of the unit has stored them (both CTAs store
+                    // rows of every tile), then order those generic stores before
+                    // this thread's TMA (async proxy) reads
                     const int32_t u = ti.u;
-                    const int32_t need = p.ph[0].n_tiles * (ti.pair ? 2 : 1);
+                    const int32_t need = p.ph[0].n_tiles * CLUSTER;
                     if (!counter_wait_bounded(p.ready + u, need, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
@@ -486,31 +503,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 }
                 const int32_t size_next = __ldg(p.sizes + e_next), pad_next = __ldg(p.padded + e_next);
                 const int32_t e_next2 = expert_of(t + 2 * n_clusters);
-                // Rows of A to load.  The odd CTA of a single block loads a box
-                // that lies wholly past the tensor's last row: it reads no
-                // memory and lands as zeros, so the discarded half of the tile
-                // multiplies zeros (on a power-capped GPU this measured ~2%
-                // faster than multiplying whatever the stage last held).  A
-                // block with at most SMALL_ROWS valid rows (decode-like) loads
-                // 16-row boxes; every other block the full 128-row box, which
-                // moves faster than many small boxes.  Rows not loaded only
-                // feed discarded rows of D.  (Only the even CTA, which sets the
-                // expected byte count, needs the odd CTA's count.)
-                auto a_boxes = [&](int32_t bx) -> int32_t {   // 0: full box
-                    int32_t r = size_cur - (bx * BM - pad_cur);
-                    r = r > BM ? BM : (r < 0 ? 0 : r);
-                    return r > SMALL_ROWS ? 0 : (r + 15) / 16;
+                // Rows of A to load, per CTA.  A pair (M = 256): this CTA's
+                // block, as one 128-row box, or as 16-row boxes when it has at
+                // most SMALL_ROWS valid rows (decode-like blocks; every other
+                // block the full box, which moves faster than many small
+                // boxes).  A lone block (M = 128): this CTA's 64 rows of it, as
+                // one 64-row box, as 16-row boxes when at most SMALL_ROWS of
+                // them are valid, or, when none is, a box that lies wholly past
+                // the tensor's last row: it reads no memory and lands as
+                // zeros, so the discarded rows multiply zeros (on a
+                // power-capped GPU zeros measured ~2% faster than whatever the
+                // stage last held).  Rows not loaded only feed discarded rows
+                // of D.  The even CTA sets the expected byte count of both.
+                struct APlan {
+                    const CUtensorMap* map;
+                    int32_t row;       // first row of the first box
+                    int32_t boxes;     // boxes per K box of the stage
+                    uint32_t bytes;    // bytes per K box
                 };
-                auto a_bytes = [&](int32_t boxes) -> uint32_t {
-                    return boxes == 0 ? A_BOX_BYTES : boxes * (A_BOX_BYTES / 8);
+                auto a_plan = [&](uint32_t r) -> APlan {
+                    if (ti.pair) {
+                        const int32_t bx = ti.bx0 + static_cast<int32_t>(r);
+                        int32_t rows = size_cur - (bx * BM - pad_cur);
+                        rows = rows > BM ? BM : (rows < 0 ? 0 : rows);
+                        if (rows > SMALL_ROWS) return APlan{a_map, bx * BM, 1, static_cast<uint32_t>(A_BOX_BYTES)};
+                        const int32_t n16 = (rows + 15) / 16;
+                        return APlan{a16_map, bx * BM, n16, n16 * A16_BYTES};
+                    }
+                    int32_t rows = size_cur - (ti.bx0 * BM - pad_cur) - static_cast<int32_t>(r) * HALF_ROWS;
+                    rows = rows > HALF_ROWS ? HALF_ROWS : (rows < 0 ? 0 : rows);
+                    const int32_t row0 = ti.bx0 * BM + static_cast<int32_t>(r) * HALF_ROWS;
+                    if (rows == 0) return APlan{a64_map, static_cast<int32_t>(p.rows_total), 1, A64_BYTES};
+                    if (rows > SMALL_ROWS) return APlan{a64_map, row0, 1, A64_BYTES};
+                    const int32_t n16 = (rows + 15) / 16;
+                    return APlan{a16_map, row0, n16, n16 * A16_BYTES};
                 };
-                const int32_t a_row = ti.store ? ti.bx * BM : static_cast<int32_t>(p.rows_total);
-                const int32_t boxes_own = ti.store ? a_boxes(ti.bx) : 0;
-                const uint32_t bytes_peer =
-                    !leader ? 0u : ti.pair ? a_bytes(a_boxes(ti.bx0 + 1)) : static_cast<uint32_t>(A_BOX_BYTES);
-                const uint32_t stage_tx = KSUB * (a_bytes(boxes_own) + bytes_peer + 2 * B_BOX_BYTES);
-                MOE_DCHECK(a_row == p.rows_total || static_cast<int64_t>(a_row) + BM <= p.rows_total, p.status);
-                MOE_DCHECK(boxes_own >= 0 && boxes_own <= SMALL_ROWS / 16, p.status);
+                const APlan own = a_plan(rank);
+                const uint32_t bytes_peer = leader ? a_plan(1).bytes : 0u;
+                const uint32_t stage_tx = KSUB * (own.bytes + bytes_peer + 2 * B_BOX_BYTES);
+                MOE_DCHECK(own.row == p.rows_total ||
+                               static_cast<int64_t>(own.row) + (own.map == a_map ? BM : own.map == a64_map
+                                                                                        ? HALF_ROWS
+                                                                                        : 16 * own.boxes) <=
+                                   p.rows_total,
+                           p.status);
+                MOE_DCHECK(own.boxes >= 1 && own.boxes <= (ti.pair ? SMALL_ROWS / 16 : HALF_ROWS / 16), p.status);
                 for (int32_t kb = 0; kb < pp.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -523,19 +560,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {
                         const int32_t k0 = (kb * KSUB + ks) * BK;
-                        if (boxes_own == 0) {
-                            tma_load_2d_pair(sa + ks * A_BOX_BYTES, a_map, fb, k0, a_row, pol_a);
+                        for (int32_t b = 0; b < own.boxes; ++b)
+                            tma_load_2d_pair(sa + ks * A_BOX_BYTES + b * A16_BYTES, own.map, fb, k0, own.row + b * 16,
+                                             pol_a);
+                        if (pt.ph == 1) {
+                            if (ti.pair) {
+                                tma_load_3d_pair(sb + ks * B_BOX_BYTES, leader ? &map_gate : &map_up, fb, k0,
+                                                 ti.n * 128, e, pol_b);
+                            } else {
+                                // this CTA's half of N: 64 gate rows, then the same 64 up rows
+                                const int32_t wrow = ti.n * 128 + static_cast<int32_t>(rank) * HALF_ROWS;
+                                tma_load_3d_pair(sb + ks * B_BOX_BYTES, &map_gate64, fb, k0, wrow, e, pol_b);
+                                tma_load_3d_pair(sb + ks * B_BOX_BYTES + B_BOX_BYTES / 2, &map_up64, fb, k0, wrow, e,
+                                                 pol_b);
+                            }
                         } else {
-                            for (int32_t b = 0; b < boxes_own; ++b)
-                                tma_load_2d_pair(sa + ks * A_BOX_BYTES + b * (A_BOX_BYTES / 8), a16_map, fb, k0,
-                                                 ti.bx * BM + b * 16, pol_a);
-                        }
-                        if (pt.ph == 1)
-                            tma_load_3d_pair(sb + ks * B_BOX_BYTES, leader ? &map_gate : &map_up, fb, k0,
-                                             ti.n * 128, e, pol_b);
-                        else
                             tma_load_3d_pair(sb + ks * B_BOX_BYTES, &map_down, fb, k0,
                                              ti.n * BN + static_cast<int32_t>(rank) * 128, e, pol_b);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -576,7 +618,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const int32_t k_blocks = p.ph[phase_of<PHASE>(t, tiles1).ph - 1].k_blocks;
+                const PhaseTile pt = phase_of<PHASE>(t, tiles1);
+                const PhaseParams& pp = p.ph[pt.ph - 1];
+                const int32_t k_blocks = pp.k_blocks;
+                const uint32_t idesc =
+                    decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank).pair ? IDESC : IDESC_M128;
                 for (int32_t kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -590,7 +636,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                         const uint32_t off = (kk / (BK / 16)) * A_BOX_BYTES + (kk % (BK / 16)) * 32;
                         const uint32_t offb = (kk / (BK / 16)) * B_BOX_BYTES + (kk % (BK / 16)) * 32;
                         tc_mma_f16_pair(d_tmem, smem_desc_k_sw128(sa + off), smem_desc_k_sw128(sb + offb),
-                                        IDESC, (kb | kk) != 0 ? 1u : 0u);
+                                        idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     // the slot may be refilled in both CTAs once these MMAs are done
                     tc_commit_pair_mc(bar_empty + 8 * stage, CLUSTER_MASK);
@@ -609,8 +655,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         __syncwarp();
     } else {
         // ===================== epilogue (warps 2..5, both CTAs) =====================
+        // A pair (M = 256): this CTA's block, row = TMEM lane, all 256 columns
+        // of N.  A lone block (M = 128): this CTA's 64 rows (rank 0: rows
+        // 0-63, rank 1: rows 64-127); lane quarters 0/1 hold rows 0-31 / 32-63
+        // with N columns 0-127 and quarters 2/3 the same rows with N columns
+        // 128-255, all in the first 128 TMEM columns of the accumulator.
         const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
-        const int row = quarter * 32 + lane;         // row of this CTA's 128-row block
         const uint32_t leader_tempty = mapa_shared(bar_tempty, 0);
         uint32_t acc = 0, aphase = 0;
         for (int32_t t = cluster_id; t < total_tiles; t += n_clusters) {
@@ -618,24 +668,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const PhaseParams& pp = p.ph[pt.ph - 1];
             const Tile ti = decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank);
             int32_t e = 0, tok = 0;
-            const int32_t actual = ti.store ? block_rows(p, ti.bx, &e, &tok) : 0;
+            const int32_t actual = block_rows(p, ti.bx, &e, &tok);
+            const int half = ti.pair ? 0 : (quarter >> 1);             // which 128 columns of N (M = 128)
+            // rows [warp_row0, warp_row0 + 32) of the block are this warp's
+            const int warp_row0 = ti.pair ? quarter * 32 : static_cast<int>(rank) * HALF_ROWS + (quarter & 1) * 32;
+            const int row = warp_row0 + lane;                            // row of the block
             if (!mbar_wait_bounded(bar_tfull + 8 * acc, aphase, abort_flag, WAIT_LIMIT_NS)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
             const int64_t grow = static_cast<int64_t>(ti.bx) * BM + row;
-            MOE_DCHECK(actual >= 0 && actual <= BM && (!ti.store || grow < p.rows_total), p.status);
+            MOE_DCHECK(actual >= 0 && actual <= BM && grow < p.rows_total, p.status);
             MOE_DCHECK(!ti.pair || actual == 0 || __ldg(p.gidx + ti.bx0) == __ldg(p.gidx + ti.bx), p.status);
-            // rows [warp_row0, warp_row0 + 32) of the block are this warp's
-            const int warp_row0 = quarter * 32;
             const int64_t wrow = static_cast<int64_t>(ti.bx) * BM + warp_row0;
             if (pt.ph == 1) {
-                uint16_t* dst_row = pp.dst + grow * pp.n_extent + static_cast<int64_t>(ti.n) * 128;
+                // gate and up of output column j: TMEM columns j and j + 128
+                // (pair), or, for this thread's half of N, columns j and j + 64
+                // (M = 128), whose outputs are columns 64*half + j of the slice
+                const int up_off = ti.pair ? 128 : 64;
+                uint16_t* dst_row = pp.dst + grow * pp.n_extent + static_cast<int64_t>(ti.n) * 128 + half * 64;
                 MOE_DCHECK(ti.n * 128 + 128 <= pp.n_extent, p.status);
 #pragma unroll 1
-                for (int c = 0; c < (warp_row0 < actual ? 4 : 0); ++c) {
+                for (int c = 0; c < (warp_row0 < actual ? up_off / 32 : 0); ++c) {
                     uint32_t g[32], u[32];
                     tmem_ld_32x32b_x32(taddr + c * 32, g);
-                    tmem_ld_32x32b_x32(taddr + 128 + c * 32, u);
+                    tmem_ld_32x32b_x32(taddr + up_off + c * 32, u);
                     tmem_ld_wait();
                     if (row < actual) {
                         uint32_t h[16];
@@ -658,16 +714,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 float w = 0.0f;
                 if (row < actual) w = __ldg(p.rw + (__ldg(p.offsets + e) + tok + row));
                 uint16_t* dst0 = pp.dst + wrow * pp.n_extent;
+                const int ncols = ti.pair ? BN : BN / 2;                 // TMEM columns this thread holds
 #pragma unroll 1
-                for (int c = 0; c < (warp_row0 < actual ? BN / 32 : 0); c += 2) {   // 64 columns per pass
-                    const int32_t col0 = ti.n * BN + c * 32;
+                for (int c = 0; c < (warp_row0 < actual ? ncols / 32 : 0); c += 2) {   // 64 columns per pass
+                    const int32_t col0 = ti.n * BN + half * (BN / 2) + c * 32;
                     MOE_DCHECK(col0 >= pp.n_extent || col0 + 64 <= pp.n_extent, p.status);
                     if (col0 >= pp.n_extent) break;             // partial last slice of H
                     uint4 el[8];
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
+                    for (int hh = 0; hh < 2; ++hh) {
                         uint32_t v[32];
-                        tmem_ld_32x32b_x32(taddr + (c + half) * 32, v);
+                        tmem_ld_32x32b_x32(taddr + (c + hh) * 32, v);
                         tmem_ld_wait();
                         uint32_t h[16];
 #pragma unroll
@@ -675,7 +732,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                             h[j] = pack_half2(__uint_as_float(v[2 * j]) * w, __uint_as_float(v[2 * j + 1]) * w);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            el[4 * half + q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                            el[4 * hh + q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
                     }
                     store_rows64(el, dst0 + col0, pp.n_extent, lane, warp_row0, actual);
                 }
@@ -693,7 +750,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 // four epilogue warps meet, then one thread releases a count.
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_THREADS) : "memory");
-                if (warp == 2 && lane == 0 && ti.store) {
+                if (warp == 2 && lane == 0) {
                     __threadfence();
                     atomicAdd(p.ready + ti.u, 1);
                 }
@@ -806,14 +863,17 @@ int64_t single_launch_workspace_bytes(int64_t num_blocks_m) {
 
 cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStream_t stream, void* ready_ws) {
     if (!encode_fn()) return cudaErrorNotSupported;
-    CUtensorMap map_x, map_x16, map_gate, map_up, map_u, map_u16, map_down;
+    CUtensorMap map_x, map_x64, map_x16, map_gate, map_up, map_gate64, map_up64, map_u, map_u64, map_u16, map_down;
     const uint64_t rows = static_cast<uint64_t>(a.rows_total);
     const uint64_t H = static_cast<uint64_t>(a.hidden), I = static_cast<uint64_t>(a.intermediate);
     const uint64_t E = static_cast<uint64_t>(a.n_experts);
-    if (!make_map_2d(&map_x, a.x, rows, H, BM) || !make_map_2d(&map_x16, a.x, rows, H, 16) ||
+    if (!make_map_2d(&map_x, a.x, rows, H, BM) || !make_map_2d(&map_x64, a.x, rows, H, HALF_ROWS) ||
+        !make_map_2d(&map_x16, a.x, rows, H, 16) ||
         !make_map_3d(&map_gate, a.gate_w, E, I, H, 128) || !make_map_3d(&map_up, a.up_w, E, I, H, 128) ||
-        !make_map_2d(&map_u, a.up_logits, rows, I, BM) || !make_map_2d(&map_u16, a.up_logits, rows, I, 16) ||
-        !make_map_3d(&map_down, a.down_w, E, H, I, 128))
+        !make_map_3d(&map_gate64, a.gate_w, E, I, H, HALF_ROWS) ||
+        !make_map_3d(&map_up64, a.up_w, E, I, H, HALF_ROWS) ||
+        !make_map_2d(&map_u, a.up_logits, rows, I, BM) || !make_map_2d(&map_u64, a.up_logits, rows, I, HALF_ROWS) ||
+        !make_map_2d(&map_u16, a.up_logits, rows, I, 16) || !make_map_3d(&map_down, a.down_w, E, H, I, 128))
         return cudaErrorInvalidValue;
 
     GemmParams p{};
@@ -882,16 +942,16 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = 2;
-        return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<3>, map_x, map_x16, map_gate, map_up, map_u, map_u16,
-                                  map_down, p);
+        return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<3>, map_x, map_x64, map_x16, map_gate, map_up,
+                                  map_gate64, map_up64, map_u, map_u64, map_u16, map_down, p);
     }
     if (flags & MOE_RUN_PHASE1) {
         const int nc = max_clusters<1>(smem);
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = 2;   // cluster + programmatic dependent launch
-        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x16, map_gate, map_up, map_x, map_x16,
-                                 map_gate, p);
+        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<1>, map_x, map_x64, map_x16, map_gate, map_up,
+                                 map_gate64, map_up64, map_x, map_x64, map_x16, map_gate, p);
         if (err != cudaSuccess) return err;
         p.drop_first_signal = 0;
     }
@@ -903,8 +963,8 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
         cfg.numAttrs = (flags & MOE_NO_PDL) ? 1 : 2;
-        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_u16, map_down, map_down, map_u, map_u16,
-                                 map_down, p);
+        err = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<2>, map_u, map_u64, map_u16, map_down, map_down,
+                                 map_down, map_down, map_u, map_u64, map_u16, map_down, p);
     }
     return err;
 }

@@ -54,13 +54,13 @@ def test_default_workload_is_the_largest():
 def test_padding_statistics_by_hand():
     """Three experts with 0, 128 and 300 rows: the "+1" rule pads them to 128,
     256 and 384 rows; their active blocks are 0, 1 and 3; the 2-SM tiles are
-    0, 1 (a lone block) and 2 (a pair plus a lone block), 256 rows each."""
+    0, 1 (a lone block, 128 rows) and 2 (a pair, 256 rows, plus a lone block)."""
     w = workloads.Workload("hand", 107, 4, 3, 256, 512)
     assert w.pairs == 428
     s = bench.work_stats(w, np.array([0, 128, 300]))
     assert s["padded_rows"] == 128 + 256 + 384
     assert s["active_blocks"] == 4 and s["tile_units"] == 3
-    assert s["executed_mma_rows"] == 3 * 256
+    assert s["executed_mma_rows"] == 128 + 256 + 128
     assert s["alloc_rows"] == (4 + 3) * 128
     assert s["padding_waste_rows"] == 7 * 128 - 428
     assert s["padded_minus_valid_rows"] == 768 - 428
