@@ -286,6 +286,32 @@ def kernel_roofline(name, flops, nbytes, ms, tc_peak, hbm_peak, tc_label, traffi
     return r
 
 
+def graph_time(fn, dev, per_graph=20, replays=10):
+    """Device time of one call of `fn` (its kernels back to back): `per_graph`
+    calls captured in a CUDA graph, replayed `replays` times after one warm
+    replay, timed with CUDA events on the capturing stream; the mean per call."""
+    import torch
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            fn()
+    g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / (replays * per_graph)
+
+
 def latency_stats(ms_list):
     import numpy as np
     a = np.asarray(ms_list, np.float64)
@@ -727,18 +753,10 @@ def main(argv=None):
                        "copies on two side streams with double-buffered staging, overlapping the "
                        "neighbouring steps' compute"}
 
-        # pack (three launches) and combine timed apart, same stream, events
-        n_pc = 50
-        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_pc)]
-        for e in pev:
-            e[0].record()
-            pack(d["ids"], d["x_tok"], d["tw"])
-            e[1].record()
-            moe.combine_routed(d["out"], prows, y=d_y[0])
-            e[2].record()
-        torch.cuda.synchronize(dev)
-        pack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in pev[n_pc // 2:])
-        combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in pev[n_pc // 2:])
+        # pack (three launches) and combine timed apart from graph replays
+        # (no host launch overhead between kernels)
+        pack_ms = graph_time(lambda: pack(d["ids"], d["x_tok"], d["tw"]), dev)
+        combine_ms = graph_time(lambda: moe.combine_routed(d["out"], prows, y=d_y[0]), dev)
 
     # ---- timing scopes of the evaluation page: the whole MoE layer ---------
     # cached_e2e: router -> dispatch -> pack -> forward -> combine on tokens
@@ -791,7 +809,7 @@ def main(argv=None):
         n_sc = max(5, min(args.steps, 100))
         cached_ms = max_over_ranks(time_fn(lambda: layer(x_l), n_sc), dist, dev)
         host_ms = max_over_ranks(time_fn(layer_host, n_sc), dist, dev)
-        router_ms = time_fn(lambda: moe.router_topk(x_l, wg, w.top_k, topk_ids=ids_l, topk_weights=tw_l), 50)
+        router_ms = graph_time(lambda: moe.router_topk(x_l, wg, w.top_k, topk_ids=ids_l, topk_weights=tw_l), dev)
         router_flops = 2.0 * w.tokens * w.hidden * w.experts
         scopes = {"routed_kernel_only_ms": ms, "cached_e2e_ms": cached_ms, "e2e_host_ms": host_ms,
                   "cached_e2e_tflops": job_value(world, flops + router_flops, cached_ms),

@@ -2,19 +2,31 @@
 // ("MetaX-TileLang工具链", §2.4: logits = W_g(x), scores = softmax(logits),
 // topk_scores, topk_indices = topk(scores)).
 //
-// One CTA per 128-token tile, one tcgen05 MMA tile of M = 128 tokens and
-// N = n_experts rounded up to 16 (at most 256), so a token's whole logit row
-// sits in one TMEM lane.  Warp 0 streams x and W_g with TMA (4 stages of
-// 64-wide K), warp 1 owns TMEM and issues the MMAs, warps 2-9 split each
-// token's row in two halves of the expert columns: per half a register top-k
-// (ties to the lower expert index, descending order) and the softmax sum
-// against the half's maximum, then the first half's thread merges the two.
+// One cluster of S CTAs per 128-token tile, one tcgen05 MMA tile of M = 128
+// tokens and N = n_experts rounded up to 16 (at most 256).  When there are
+// fewer tiles than SMs the tile's K (hidden) is split over the S CTAs of its
+// cluster, so that tiles x S SMs stream x instead of one per tile.  Warp 0
+// streams the CTA's K range of x and W_g with TMA (4 stages of 64-wide K),
+// warp 1 owns TMEM and issues the MMAs, warps 2-17 are the epilogue:
+//  1. CTA r of the cluster owns tokens r*128/S .. (r+1)*128/S - 1 of the
+//     tile.  Every CTA stores its fp32 logits (partial sums over its K range
+//     when S > 1) from TMEM into its owners' shared memory, one slot per
+//     source CTA (distributed shared memory stores, no round trips);
+//  2. after a cluster barrier each owner sums the S slots of its tokens in
+//     rank order, one warp per token with the experts spread over the lanes
+//     (expert e in lane e % 32): a butterfly maximum, a butterfly sum of
+//     exp(l - max), and the top-k as k rounds of a butterfly arg-max
+//     (descending logit, ties to the lower expert index); lane q writes the
+//     q-th choice.
 // The top-k is decided on the logits (softmax preserves their order).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <utility>
 
 #include "../../include/moe_gb300.h"
 #include "moe_internal.h"
@@ -29,19 +41,19 @@ constexpr int R_STAGES = 4;
 constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB
 constexpr int R_B_MAX_BYTES = 256 * R_BK * 2;        // 32 KB
 constexpr int R_STAGE_BYTES = R_A_BYTES + R_B_MAX_BYTES;
-constexpr int R_THREADS = 320;                       // producer, MMA, 8 epilogue warps
-constexpr int R_EPI_THREADS = 256;
-constexpr int R_MAX_TOPK = 16;
+constexpr int R_EPI_WARPS = 16;
+constexpr int R_THREADS = 64 + 32 * R_EPI_WARPS;     // producer, MMA, epilogue warps
+constexpr int R_MAX_E = 256;                         // MOE_ROUTER_MAX_EXPERTS
+constexpr int R_VPL = R_MAX_E / 32;                  // logits per lane of a token's warp, at most
 constexpr uint64_t R_WAIT_NS = 2000000000ull;
 constexpr uint64_t R_DRAIN_NS = 200000000ull;
 constexpr int R_OFF_BARS = R_STAGES * R_STAGE_BYTES;
 constexpr int R_OFF_TMEM = R_OFF_BARS + (2 * R_STAGES + 2) * 8;
 constexpr int R_OFF_ABORT = R_OFF_TMEM + 4;
-// the second half-row's partial results, handed to the first half's thread:
-// top-k values [R_MAX_TOPK][128], ids [R_MAX_TOPK][128], max [128], sum [128]
-constexpr int R_OFF_XCH = ((R_OFF_ABORT + 4 + 15) / 16) * 16;
-constexpr int R_XCH_BYTES = (2 * R_MAX_TOPK + 2) * R_BM * 4;
-constexpr size_t R_SMEM = 1024 + R_OFF_XCH + R_XCH_BYTES;
+constexpr size_t R_SMEM = 1024 + R_OFF_ABORT + 16;
+constexpr int R_MAX_SPLIT = 8;   // CTAs per cluster (the portable cluster size)
+
+static_assert(R_MAX_E == MOE_ROUTER_MAX_EXPERTS, "router expert limit");
 
 struct RouterParams {
     int64_t n_tokens;
@@ -55,6 +67,13 @@ struct RouterParams {
     int32_t* status;
 };
 
+// (l, e) ranks above (lo, eo): a larger logit, or an equal one with a lower expert index
+__device__ __forceinline__ bool ranks_above(float l, int32_t e, float lo, int32_t eo) {
+    return l > lo || (l == lo && e < eo);
+}
+
+// S: CTAs per cluster (1, 2, 4 or 8); CTA r runs K blocks k_blocks*r/S .. k_blocks*(r+1)/S.
+template <int S>
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
               const RouterParams p) {
@@ -93,7 +112,17 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int32_t row0 = static_cast<int32_t>(blockIdx.x) * R_BM;
+    const uint32_t rank = S > 1 ? cluster_cta_rank() : 0u;
+    const int32_t row0 = static_cast<int32_t>(blockIdx.x / S) * R_BM;
+    const int32_t kb_begin = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * rank) / S);
+    const int32_t kb_end = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (rank + 1)) / S);
+    // The owner's slots, in the stage area (free once the cluster's MMAs have
+    // all completed): slot of source CTA s, expert e, owned token j at
+    // (s * n_pad + e) * RS + j; the odd row stride RS keeps a token's warp,
+    // which reads 32 consecutive experts, on 32 banks.
+    constexpr int ROWS = R_BM / S;                       // tokens a CTA owns
+    constexpr int RS = ROWS + 1;
+    float* slots = reinterpret_cast<float*>(smem);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -101,7 +130,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+            for (int32_t kb = kb_begin; kb < kb_end; ++kb) {
                 if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, R_WAIT_NS)) {
                     ok = false;
                     break;
@@ -130,7 +159,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
             const uint32_t idesc = idesc_f16_f32acc(R_BM, static_cast<uint32_t>(p.n_pad));
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+            for (int32_t kb = kb_begin; kb < kb_end; ++kb) {
                 if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, R_WAIT_NS)) {
                     ok = false;
                     break;
@@ -141,7 +170,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < R_BK / 16; ++kk)
                     tc_mma_f16(tmem_base, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32), idesc,
-                               (kb | kk) != 0 ? 1u : 0u);
+                               (kb != kb_begin || kk != 0) ? 1u : 0u);
                 tc_commit(bar_empty + 8 * stage);
                 if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -152,112 +181,118 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         }
         __syncwarp();
     } else {
-        // Warps 2-9: warp w reads TMEM lanes 32*(w%4) .. +31 (one token per
-        // thread); warps 2-5 take the first half of the expert columns and
-        // warps 6-9 the second half, then the second half's thread hands its
-        // partial top-k, max and sum to the first half's thread of the same
-        // token, which merges them and writes the token's outputs.
+        if (mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS)) tc_fence_after_sync();
+        __syncwarp();
+    }
+    // every CTA of the cluster has finished its MMAs (its stage area is free)
+    if (S > 1) cluster_sync_all();
+    else __syncthreads();
+
+    if (warp >= 2 && !*abort_flag) {
+        // step 1: TMEM -> the owners' slots.  Warp w reads TMEM lanes
+        // 32*(w%4) .. +31 (one token each); the four warps of a lane quarter
+        // take every fourth group of 8 columns.
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int cpart = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
-        const int64_t t = static_cast<int64_t>(row0) + row;
-        const int32_t n_half = p.n_pad / 2;              // a multiple of 8
-        const int32_t c_begin = half * n_half;
-        float* xv = reinterpret_cast<float*>(smem + R_OFF_XCH);
-        int32_t* xi = reinterpret_cast<int32_t*>(xv + R_MAX_TOPK * R_BM);
-        float* xm = reinterpret_cast<float*>(xi + R_MAX_TOPK * R_BM);
-        float* xs = xm + R_BM;
-        float best_v[R_MAX_TOPK];
-        int32_t best_i[R_MAX_TOPK];
+        const int owner = row / ROWS;
+        const uint32_t dst = (S > 1 ? mapa_shared(smem_u32(slots), static_cast<uint32_t>(owner)) : smem_u32(slots)) +
+                             4u * static_cast<uint32_t>(static_cast<int>(rank) * p.n_pad * RS + (row - owner * ROWS));
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        for (int32_t c0 = 8 * cpart; c0 < p.n_pad; c0 += 32) {
+            uint32_t v[8];
+            tmem_ld_32x32b_x8(taddr + c0, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < R_MAX_TOPK; ++q) {
-            best_v[q] = -INFINITY;
-            best_i[q] = -1;
-        }
-        float s = 0.0f;
-        // Insert (l, e) into the descending list (everything in registers: all
-        // loops over the list are unrolled with compile-time indices).  A new
-        // value goes in after any equal one, so the lower expert index stays
-        // first, and every slot is updated from the old list at once.
-        auto insert = [&](float l, int32_t e) {
-            bool gt[R_MAX_TOPK];
-#pragma unroll
-            for (int q = 0; q < R_MAX_TOPK; ++q) gt[q] = best_i[q] < 0 || l > best_v[q];
-#pragma unroll
-            for (int q = R_MAX_TOPK - 1; q > 0; --q) {
-                best_v[q] = gt[q - 1] ? best_v[q - 1] : (gt[q] ? l : best_v[q]);
-                best_i[q] = gt[q - 1] ? best_i[q - 1] : (gt[q] ? e : best_i[q]);
-            }
-            if (gt[0]) {
-                best_v[0] = l;
-                best_i[0] = e;
-            }
-        };
-        const bool ok = mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS);
-        if (ok) {
-            tc_fence_after_sync();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            // pass 1: the R_MAX_TOPK largest logits of this half (8 columns per
-            // TMEM load keeps the unrolled code within the instruction cache)
-            for (int32_t c0 = c_begin; c0 < c_begin + n_half; c0 += 8) {
-                uint32_t v[8];
-                tmem_ld_32x32b_x8(taddr + c0, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int32_t e = c0 + j;
-                    const float l = __uint_as_float(v[j]);
-                    if (e < p.n_experts && (best_i[R_MAX_TOPK - 1] < 0 || l > best_v[R_MAX_TOPK - 1])) insert(l, e);
-                }
-            }
-            // pass 2: sum of exp(l - this half's max), independent partial sums
-            const float mh = best_v[0];
-            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            for (int32_t c0 = c_begin; c0 < c_begin + n_half; c0 += 8) {
-                uint32_t v[8];
-                tmem_ld_32x32b_x8(taddr + c0, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (c0 + j < p.n_experts) part[j & 3] += expf(__uint_as_float(v[j]) - mh);
-            }
-            s = (part[0] + part[1]) + (part[2] + part[3]);
-            if (half == 1) {
-#pragma unroll
-                for (int q = 0; q < R_MAX_TOPK; ++q) {
-                    xv[q * R_BM + row] = best_v[q];
-                    xi[q * R_BM + row] = best_i[q];
-                }
-                xm[row] = mh;
-                xs[row] = s;
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t a = dst + 4u * static_cast<uint32_t>((c0 + j) * RS);
+                if (S > 1) st_shared_cluster_f32(a, __uint_as_float(v[j]));
+                else slots[(c0 + j) * RS + row] = __uint_as_float(v[j]);
             }
         }
-        // every epilogue thread meets here, whatever its wait returned
-        asm volatile("bar.sync 1, %0;" ::"r"(R_EPI_THREADS) : "memory");
-        if (half == 0 && ok && !*abort_flag) {
-            // merge: the other half's experts all have higher indices, so its
-            // entries go after equal values already in the list
-            const float m0 = best_v[0], m1 = xm[row];
-            for (int q = 0; q < R_MAX_TOPK; ++q) {
-                const int32_t e = xi[q * R_BM + row];
-                const float l = xv[q * R_BM + row];
-                if (e < 0) break;
-                if (best_i[R_MAX_TOPK - 1] >= 0 && !(l > best_v[R_MAX_TOPK - 1])) break;
-                insert(l, e);
-            }
-            const float mx = best_v[0];                   // = max(m0, m1)
-            const float st = s * expf(m0 - mx) + (m1 == -INFINITY ? 0.0f : xs[row] * expf(m1 - mx));
-            if (t < p.n_tokens) {
+    }
+    // every slot is written (and every CTA's abort flag is final)
+    tc_fence_before_sync();
+    __syncwarp();
+    if (S > 1) cluster_sync_all();
+    else __syncthreads();
+
+    if (warp >= 2) {
+        bool ok = true;
+        const uint32_t abort_addr = smem_u32(const_cast<int*>(abort_flag));
 #pragma unroll
-                for (int q = 0; q < R_MAX_TOPK; ++q) {
-                    if (q < p.top_k) {
-                        // ids in range and the list in descending order
-                        MOE_DCHECK(best_i[q] >= 0 && best_i[q] < p.n_experts, p.status);
-                        MOE_DCHECK(q == 0 || !(best_v[q] > best_v[q > 0 ? q - 1 : 0]), p.status);
-                        p.topk_ids[t * p.top_k + q] = best_i[q];
-                        p.topk_weights[t * p.top_k + q] = expf(best_v[q] - mx) / st;
+        for (int r = 0; r < S; ++r)
+            if ((S > 1 ? ld_shared_cluster_s32(mapa_shared(abort_addr, static_cast<uint32_t>(r))) : *abort_flag) != 0)
+                ok = false;
+        // step 2: one warp per owned token
+        for (int j = warp - 2; ok && j < ROWS; j += R_EPI_WARPS) {
+            const int64_t t = static_cast<int64_t>(row0) + static_cast<int>(rank) * ROWS + j;
+            if (t >= p.n_tokens) break;
+            float l[R_VPL];
+#pragma unroll
+            for (int i = 0; i < R_VPL; ++i) {
+                const int32_t e = lane + 32 * i;
+                float v = -INFINITY;
+                if (e < p.n_experts) {
+                    v = 0.0f;
+#pragma unroll
+                    for (int s = 0; s < S; ++s) v += slots[(s * p.n_pad + e) * RS + j];
+                }
+                l[i] = v;
+            }
+            // maximum and sum of exp(l - max) over the token's experts
+            float m = l[0];
+#pragma unroll
+            for (int i = 1; i < R_VPL; ++i) m = fmaxf(m, l[i]);
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < R_VPL; ++i)
+                if (lane + 32 * i < p.n_experts) sum += expf(l[i] - m);
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+            sum = __shfl_sync(0xffffffffu, sum, 0);         // one value for every lane
+            // top-k: k rounds of a butterfly arg-max over (logit desc, expert asc)
+            int32_t my_id = -1;
+            float my_w = 0.0f;
+            for (int q = 0; q < p.top_k; ++q) {
+                float bv = -INFINITY;
+                int32_t be = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < R_VPL; ++i) {
+                    const int32_t e = lane + 32 * i;
+                    if (e < p.n_experts && l[i] != -INFINITY && ranks_above(l[i], e, bv, be)) {
+                        bv = l[i];
+                        be = e;
                     }
                 }
+#pragma unroll
+                for (int d = 16; d >= 1; d >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+                    const int32_t oe = __shfl_xor_sync(0xffffffffu, be, d);
+                    if (ranks_above(ov, oe, bv, be)) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                // every lane holds the winner; its own lane retires it
+                if ((be & 31) == lane) {
+#pragma unroll
+                    for (int i = 0; i < R_VPL; ++i)
+                        if (lane + 32 * i == be) l[i] = -INFINITY;
+                }
+                if (lane == q) {
+                    // no finite logit left (NaN inputs): no expert
+                    my_id = be == 0x7fffffff ? -1 : be;
+                    my_w = expf(bv - m) / sum;
+                }
+            }
+            if (lane < p.top_k) {
+                // an id in range (a finite logit was found for this rank)
+                MOE_DCHECK(my_id >= 0 && my_id < p.n_experts, p.status);
+                p.topk_ids[t * p.top_k + lane] = my_id;
+                p.topk_weights[t * p.top_k + lane] = my_w;
             }
         }
     }
@@ -325,12 +360,51 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
         !router_map(&map_w, router_w, static_cast<uint64_t>(n_experts), static_cast<uint64_t>(hidden),
                     static_cast<uint32_t>(p.n_pad)))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(R_SMEM));
-    if (err != cudaSuccess) return err;
-    const unsigned grid = static_cast<unsigned>((n_tokens + R_BM - 1) / R_BM);
-    router_kernel<<<grid, R_THREADS, R_SMEM, stream>>>(map_x, map_w, p);
-    return cudaGetLastError();
+    const int64_t tiles = (n_tokens + R_BM - 1) / R_BM;
+    // K split: the largest power of two S <= R_MAX_SPLIT with tiles x S
+    // within the SM count and at most one CTA per 64-wide K block
+    int64_t split = 1;
+    while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks) split *= 2;
+    auto kernel_for = [](int64_t s) {
+        return s >= 8 ? router_kernel<8> : s == 4 ? router_kernel<4> : s == 2 ? router_kernel<2> : router_kernel<1>;
+    };
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(R_THREADS);
+    cfg.dynamicSmemBytes = R_SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a cluster size the device can place (clusters live inside one GPC);
+    // the answer is cached per device and size
+    static std::mutex mu;
+    static std::map<std::pair<int, int64_t>, bool> placeable;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNoDevice;
+    for (; split >= 1; split /= 2) {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto key = std::make_pair(dev, split);
+        auto it = placeable.find(key);
+        if (it == placeable.end()) {
+            cudaError_t e = cudaFuncSetAttribute(kernel_for(split), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(R_SMEM));
+            if (e != cudaSuccess) return e;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+            cfg.gridDim = dim3(static_cast<unsigned>(split));
+            int n = 0;
+            const bool ok = split == 1 || (cudaOccupancyMaxActiveClusters(&n, kernel_for(split), &cfg) == cudaSuccess &&
+                                           n > 0);
+            if (!ok) cudaGetLastError();
+            it = placeable.emplace(key, ok).first;
+        }
+        if (it->second) break;
+    }
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
+    return cudaLaunchKernelEx(&cfg, kernel_for(split), map_x, map_w, p);
 }
 
 }  // namespace moe
