@@ -82,7 +82,7 @@ constexpr uint32_t IDESC_M128 = idesc_f16_f32acc(BM, BN);  // M = 128 across the
 constexpr int HALF_ROWS = BM / 2;                          // rows of a lone block each CTA holds
 constexpr uint32_t A16_BYTES = A_BOX_BYTES / 8;            // a 16-row box of A
 constexpr uint32_t A64_BYTES = A_BOX_BYTES / 2;            // a 64-row box of A
-constexpr int64_t GROUP_A_BYTES = 32ll << 20;     // A rows a tile-order group keeps hot in L2
+constexpr int64_t GROUP_A_BYTES = 64ll << 20;     // A rows a tile-order group keeps hot in L2
 constexpr int32_t UNITS_PER_EXPERT_MULT = 1;
 
 static_assert(MOE_MAX_BLOCKS <= 0x7FFF, "block indices must leave the pair bit free");
@@ -94,13 +94,16 @@ constexpr int OFF_BARS = STAGES * STAGE_BYTES;                 // 8-byte mbarrie
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;               // full, empty, tfull, tempty, drain
 constexpr int OFF_TMEM_SLOT = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
-constexpr int OFF_COUNTS = OFF_ABORT + 4;                      // nact, nunits
-constexpr int OFF_WSUM = OFF_COUNTS + 8;                       // NUM_THREADS/32 ints
+constexpr int OFF_COUNTS = OFF_ABORT + 4;                      // runs, units, groups, (spare)
+constexpr int OFF_WSUM = OFF_COUNTS + 16;                      // NUM_THREADS/32 ints
 constexpr int OFF_UNITS = ((OFF_WSUM + (NUM_THREADS / 32) * 4 + 15) / 16) * 16;
 
+// After the unit list (one uint16 per unit, at most one unit per block)
+// comes, when the tile order uses per-expert groups, the first unit of every
+// group (one uint16 per group, at most one group per unit).
 __host__ __device__ inline size_t units_bytes(int64_t m) { return ((2 * static_cast<size_t>(m) + 15) / 16) * 16; }
-size_t smem_bytes_for(int64_t m) {
-    return 1024 /* alignment slack */ + OFF_UNITS + units_bytes(m) + (MOE_DEBUG ? 16 : 0);
+size_t smem_bytes_for(int64_t m, bool expert_groups) {
+    return 1024 /* alignment slack */ + OFF_UNITS + units_bytes(m) * (expert_groups ? 2 : 1) + (MOE_DEBUG ? 16 : 0);
 }
 constexpr uint32_t SMEM_CANARY = 0xC0FFEE11u;
 
@@ -109,7 +112,7 @@ struct PhaseParams {
     int32_t k_blocks;         // K / (64 * KSUB)
     int32_t n_tiles;          // N slices per block
     int32_t n_extent;         // I (phase 1) or H (phase 2): columns of dst
-    int32_t group;            // largest group of the tile order the L2 budget allows (>= 1)
+    int32_t group;            // most units of a tile-order group the L2 budget allows (>= 1)
 };
 
 struct GemmParams {
@@ -129,6 +132,7 @@ struct GemmParams {
     int32_t* ready;           // both phases in one launch: per unit, finished phase-1 tile stores
                               // (zero at launch)
     int32_t drop_first_signal;   // failure-path test: skip the first "accumulator ready" commit
+    int32_t expert_groups;    // one-phase launches: tile-order groups follow the experts (see decode_tile_groups)
 };
 
 // Rows of block bx that belong to its expert ("Fused MoE GEMM 提交说明",
@@ -159,11 +163,15 @@ __device__ __forceinline__ int32_t block_rows(const GemmParams& p, int32_t bx, i
 }
 
 // One cluster tile as seen by the CTA of rank `rank`.  Tile order: the unit
-// list (expert-sorted) is cut into groups of `group` consecutive units, and
-// inside a group the tiles run slice by slice, each slice over all the
-// group's units.  Concurrent clusters then share each weight slice across an
-// expert's units while the group's A rows stay in L2; group = 1 is plain
-// unit-major order.
+// list (expert-sorted) is cut into groups of consecutive units, and inside a
+// group the tiles run slice by slice, each slice over all the group's units.
+// Concurrent clusters then share each weight slice across an expert's units
+// while the group's A rows stay in L2.  decode_tile: groups of `group` units
+// (about the average number of units per expert; group = 1 is plain
+// unit-major order).  decode_tile_groups: groups that follow the experts,
+// each expert's units split evenly into as few groups as the L2 budget
+// allows, so an expert with many units streams its weights a few times
+// instead of once per average-sized group.
 struct Tile {
     int32_t u;        // unit
     int32_t bx0;      // first block of the unit (the expert comes from it)
@@ -182,6 +190,28 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const uint16_t* units, in
     Tile ti;
     ti.n = l / gsize;
     const int32_t u = g * group + (l - ti.n * gsize);
+    ti.u = u;
+    ti.bx0 = units[u] & 0x7FFF;
+    ti.pair = (units[u] & PAIR_BIT) != 0;
+    ti.bx = ti.pair ? ti.bx0 + static_cast<int32_t>(rank) : ti.bx0;
+    return ti;
+}
+
+// Group g starts at unit gstart[g] and its tiles at gstart[g] * n_tiles.
+__device__ __forceinline__ Tile decode_tile_groups(int32_t t, const uint16_t* units, const uint16_t* gstart,
+                                                   int32_t ngroups, int32_t n_tiles, int32_t nunits, uint32_t rank) {
+    int32_t lo = 0, hi = ngroups - 1;            // the last group that starts at or before tile t
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (static_cast<int32_t>(gstart[mid]) * n_tiles <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const int32_t g0 = gstart[lo];
+    const int32_t gsize = (lo + 1 < ngroups ? static_cast<int32_t>(gstart[lo + 1]) : nunits) - g0;
+    const int32_t l = t - g0 * n_tiles;
+    Tile ti;
+    ti.n = l / gsize;
+    const int32_t u = g0 + (l - ti.n * gsize);
     ti.u = u;
     ti.bx0 = units[u] & 0x7FFF;
     ti.pair = (units[u] & PAIR_BIT) != 0;
@@ -314,6 +344,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     // prologue scratch in the (still unused) stage area
     uint16_t* act_bx = reinterpret_cast<uint16_t*>(smem + OFF_STAGES);
     uint16_t* act_e = act_bx + p.num_blocks_m;
+    uint16_t* unit_rs = act_e + p.num_blocks_m;            // each unit's run (its first list entry)
+    uint16_t* unit_pos = unit_rs + p.num_blocks_m;         // and its position among the run's units
+    uint16_t* run_nb = unit_pos + p.num_blocks_m;          // at a run's first entry: the run's blocks
+    uint16_t* gstart = units + units_bytes(p.num_blocks_m) / 2;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -397,6 +431,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     // positions start a unit, which is a pair when the run continues.
     if (warp == 0) {
         int32_t nu = 0, run_start = 0, nruns = 0;
+        int32_t run_min = 0x7fffffff, run_max = 0;          // units per run (this lane's run ends)
         for (int32_t base = 0; base < nact; base += 32) {
             const int32_t i = base + lane;
             const bool in = i < nact;
@@ -409,23 +444,93 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             const bool ustart = in && (((i - rs) & 1) == 0);
             const bool next_cont = (i + 1 < nact) && act_e[i + 1] == ei && act_bx[i + 1] == bxi + 1;
             const uint32_t ub = __ballot_sync(0xffffffffu, ustart);
-            if (ustart)
-                units[nu + __popc(ub & ((1u << lane) - 1u))] =
-                    static_cast<uint16_t>(bxi | (next_cont ? PAIR_BIT : 0));
+            if (ustart) {
+                const int32_t idx = nu + __popc(ub & ((1u << lane) - 1u));
+                units[idx] = static_cast<uint16_t>(bxi | (next_cont ? PAIR_BIT : 0));
+                unit_rs[idx] = static_cast<uint16_t>(rs);
+                unit_pos[idx] = static_cast<uint16_t>((i - rs) >> 1);
+            }
+            if (in && !next_cont) {                           // the run ends here
+                run_nb[rs] = static_cast<uint16_t>(i - rs + 1);
+                const int32_t ru = (i - rs + 2) >> 1;
+                run_min = ru < run_min ? ru : run_min;
+                run_max = ru > run_max ? ru : run_max;
+            }
             nu += __popc(ub);
             nruns += __popc(starts);
             if (starts) run_start = base + 31 - __clz(starts);
         }
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) {
+            const int32_t a = __shfl_xor_sync(0xffffffffu, run_min, d);
+            const int32_t b = __shfl_xor_sync(0xffffffffu, run_max, d);
+            run_min = a < run_min ? a : run_min;
+            run_max = b > run_max ? b : run_max;
+        }
         if (lane == 0) {
             counts[0] = nruns;
             counts[1] = nu;
+            counts[2] = 0;
+            // every run has the same number of units, within the L2 budget:
+            // per-expert groups are the runs, which the fixed-size order
+            // with groups of about one run already gives
+            counts[3] = run_min == run_max && run_max <= p.ph[PHASE == 2 ? 1 : 0].group ? -1 : 0;
         }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    if (PHASE != 3 && p.expert_groups && counts[3] == 0) {
+        // ---- 3. per-expert groups of the tile order -------------------------
+        // A run's (an expert's) n units are split evenly into k = ceil(n / cap)
+        // groups: group j starts at its unit floor(j * n / k).  Every thread
+        // flags the units that start a group; the flags are compacted in unit
+        // order.  When every group has the same size the cheaper fixed-size
+        // decode gives the same order and is used instead.
+        const int32_t cap = p.ph[PHASE == 2 ? 1 : 0].group;
+        const int32_t nu = counts[1];
+        int32_t ng = 0;
+        for (int32_t base = 0; base < nu; base += NUM_THREADS) {
+            const int32_t u = base + tid;
+            int32_t flag = 0;
+            if (u < nu) {
+                const int32_t pos = unit_pos[u];
+                const int32_t n = (run_nb[unit_rs[u]] + 1) >> 1;                 // the run's units
+                flag = u == 0 || pos == 0;
+                if (!flag && pos < n) {
+                    const int32_t k = (n + cap - 1) / cap;
+                    const int32_t j = (pos * k + n - 1) / n;                     // first group at or after pos
+                    flag = j < k && (j * n) / k == pos;
+                }
+            }
+            const uint32_t ballot = __ballot_sync(0xffffffffu, flag);
+            if (lane == 0) wsum[warp] = __popc(ballot);
+            __syncthreads();
+            int32_t before = 0, total = 0;
+#pragma unroll
+            for (int w = 0; w < NUM_THREADS / 32; ++w) {
+                const int32_t c = wsum[w];
+                before += (w < warp) ? c : 0;
+                total += c;
+            }
+            if (flag) gstart[ng + before + __popc(ballot & ((1u << lane) - 1u))] = static_cast<uint16_t>(u);
+            ng += total;
+            __syncthreads();
+        }
+        const int32_t g0 = ng >= 2 ? gstart[1] : nu;                             // the first group's size
+        int32_t same = 1;
+        for (int32_t g = tid; g < ng; g += NUM_THREADS)
+            if (gstart[g] != g * g0) same = 0;
+        same = __syncthreads_and(same) && nu - (ng - 1) * g0 <= g0;
+        if (tid == 0) {
+            counts[2] = same ? 0 : ng;
+            counts[3] = same ? g0 : 0;
+        }
+        __syncthreads();
+    }
     const uint32_t tmem_base = *tmem_slot;
-    volatile uint32_t* canary = reinterpret_cast<volatile uint32_t*>(smem + OFF_UNITS + units_bytes(p.num_blocks_m));
+    volatile uint32_t* canary = reinterpret_cast<volatile uint32_t*>(
+        smem + OFF_UNITS + units_bytes(p.num_blocks_m) * (PHASE != 3 && p.expert_groups ? 2 : 1));
     if (MOE_DEBUG && tid == 0) *canary = SMEM_CANARY;
     MOE_DCHECK(counts[1] <= p.num_blocks_m && counts[0] <= counts[1], p.status);
     const int32_t tiles1 = PHASE == 2 ? 0 : counts[1] * p.ph[0].n_tiles;
@@ -439,8 +544,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     // Tile-order group: about one expert's units (so a weight slice is shared
     // by all of them at once), at most what the host's L2 budget allows.
     const int32_t upe = counts[0] > 0 ? UNITS_PER_EXPERT_MULT * ((counts[1] + counts[0] - 1) / counts[0]) : 1;
-    const int32_t grp[2] = {p.ph[0].group < upe ? p.ph[0].group : upe,
-                            p.ph[1].group < upe ? p.ph[1].group : upe};
+    int32_t grp[2] = {p.ph[0].group < upe ? p.ph[0].group : upe, p.ph[1].group < upe ? p.ph[1].group : upe};
+    if (PHASE != 3 && p.expert_groups && counts[3] > 0) grp[PHASE - 1] = counts[3];   // equal per-expert groups
+    const int32_t ngroups = counts[2];
+    MOE_DCHECK(ngroups == 0 || (ngroups <= counts[1] && gstart[0] == 0), p.status);
+    auto tile_of = [&](const PhaseTile& pt) -> Tile {
+        const PhaseParams& q = p.ph[pt.ph - 1];
+        return ngroups > 0 ? decode_tile_groups(pt.t, units, gstart, ngroups, q.n_tiles, counts[1], rank)
+                           : decode_tile(pt.t, units, q.n_tiles, counts[1], grp[pt.ph - 1], rank);
+    };
     // Both CTAs' barriers are initialised and their prologue scratch in the
     // stage area is dead before either CTA's copies or commits reach the other.
     cluster_sync_all();
@@ -468,8 +580,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             auto expert_of = [&](int32_t tt) -> int32_t {
                 if (tt >= total_tiles) return 0;
                 const PhaseTile pt = phase_of<PHASE>(tt, tiles1);
-                const PhaseParams& q = p.ph[pt.ph - 1];
-                return __ldg(p.gidx + decode_tile(pt.t, units, q.n_tiles, counts[1], grp[pt.ph - 1], rank).bx0);
+                return __ldg(p.gidx + tile_of(pt).bx0);
             };
             int32_t e_cur = expert_of(cluster_id);
             int32_t size_cur = __ldg(p.sizes + e_cur), pad_cur = __ldg(p.padded + e_cur);
@@ -477,7 +588,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
             for (int32_t t = cluster_id; t < total_tiles && ok; t += n_clusters) {
                 const PhaseTile pt = phase_of<PHASE>(t, tiles1);
                 const PhaseParams& pp = p.ph[pt.ph - 1];
-                const Tile ti = decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank);
+                const Tile ti = tile_of(pt);
                 const int32_t e = e_cur;
                 MOE_DCHECK(ti.u >= 0 && ti.u < counts[1] && ti.n >= 0 && ti.n < pp.n_tiles, p.status);
                 MOE_DCHECK(ti.bx >= 0 && ti.bx < p.num_blocks_m && e >= 0 && e < p.n_experts, p.status);
@@ -621,8 +732,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
                 const PhaseTile pt = phase_of<PHASE>(t, tiles1);
                 const PhaseParams& pp = p.ph[pt.ph - 1];
                 const int32_t k_blocks = pp.k_blocks;
-                const uint32_t idesc =
-                    decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank).pair ? IDESC : IDESC_M128;
+                const uint32_t idesc = tile_of(pt).pair ? IDESC : IDESC_M128;
                 for (int32_t kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, WAIT_LIMIT_NS)) {
                         ok = false;
@@ -666,7 +776,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
         for (int32_t t = cluster_id; t < total_tiles; t += n_clusters) {
             const PhaseTile pt = phase_of<PHASE>(t, tiles1);
             const PhaseParams& pp = p.ph[pt.ph - 1];
-            const Tile ti = decode_tile(pt.t, units, pp.n_tiles, counts[1], grp[pt.ph - 1], rank);
+            const Tile ti = tile_of(pt);
             int32_t e = 0, tok = 0;
             const int32_t actual = block_rows(p, ti.bx, &e, &tok);
             const int half = ti.pair ? 0 : (quarter >> 1);             // which 128 columns of N (M = 128)
@@ -908,15 +1018,25 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
     p.ready = static_cast<int32_t*>(ready_ws);
     p.drop_first_signal = (flags & MOE_TEST_DROP_SIGNAL) ? 1 : 0;
 
-    const size_t smem = smem_bytes_for(a.num_blocks_m);
+    // One-phase launches order their tiles in per-expert groups when the
+    // group table fits in shared memory beside the unit list (up to several
+    // thousand blocks); otherwise, and for the single launch, in groups of
+    // the average units per expert.
+    int dev = 0, max_smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return cudaErrorNoDevice;
+    const bool groups_fit = smem_bytes_for(a.num_blocks_m, true) <= static_cast<size_t>(max_smem);
+    const size_t smem = smem_bytes_for(a.num_blocks_m, groups_fit);
+    const size_t smem3 = smem_bytes_for(a.num_blocks_m, false);
+    p.expert_groups = groups_fit ? 1 : 0;
     cudaError_t err = cudaSuccess;
-    const int smem_i = static_cast<int>(smem);
-    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_i)) !=
-            cudaSuccess ||
-        (err = cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_i)) !=
-            cudaSuccess ||
-        (err = cudaFuncSetAttribute(grouped_gemm_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_i)) !=
-            cudaSuccess)
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem))) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem))) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem3))) != cudaSuccess)
         return err;
 
     cudaLaunchAttribute attr[2];
@@ -938,10 +1058,12 @@ cudaError_t launch_fused_forward(const ForwardArgs& a, uint32_t flags, cudaStrea
         err = cudaMemsetAsync(ready_ws, 0, static_cast<size_t>(single_launch_workspace_bytes(a.num_blocks_m)),
                               stream);
         if (err != cudaSuccess) return err;
-        const int nc = max_clusters<3>(smem);
+        const int nc = max_clusters<3>(smem3);
         if (nc <= 0) return cudaErrorNoDevice;
         cfg.gridDim = dim3(static_cast<unsigned>(CLUSTER * nc));
+        cfg.dynamicSmemBytes = smem3;
         cfg.numAttrs = 2;
+        p.expert_groups = 0;
         return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<3>, map_x, map_x64, map_x16, map_gate, map_up,
                                   map_gate64, map_up64, map_u, map_u64, map_u16, map_down, p);
     }

@@ -3,7 +3,7 @@
 This module serves both the CUDA path and the CPU oracle, so it holds none of
 the method's arithmetic: no dispatch tables, no packing, no GEMM.  It draws
 routing choices, routed weights, token activations and expert weights with the
-shapes and distributions of the five workloads below, and nothing else.
+shapes and distributions of the workloads below, and nothing else.
 
 Workloads (model-shaped; no dataset or trained weights are involved):
   tiny            64 tokens, top-2 of 4 experts, hidden 256, intermediate 512,
@@ -12,6 +12,8 @@ Workloads (model-shaped; no dataset or trained weights are involved):
   mixtral         Mixtral-shaped: 8192 tokens, top-2 of 8, 4096 / 14336, uniform
   decode_skewed   32 tokens, top-8 of 128, 2048 / 768, Zipf(s=1.2) popularity
   dsv3            DeepSeek-V3-shaped: 16384 tokens, top-8 of 256, 7168 / 2048, Zipf(s=1.0)
+  dsv3_slice      a small case of the DeepSeek-V3-shaped kernels for profiler captures
+                  (a few GB on the device): 2048 tokens, top-8 of 32, 7168 / 2048, Zipf(s=1.0)
 
 Distributions: x ~ N(0, 1) fp16; gate/up ~ N(0, 1/hidden), down ~ N(0, 1/intermediate)
 fp16 (tiny: all three ~ N(0, 1/hidden)); routed weights = softmax over the k
@@ -55,6 +57,7 @@ WORKLOADS = {
     "mixtral": Workload("mixtral", 8192, 2, 8, 4096, 14336, "uniform"),
     "decode_skewed": Workload("decode_skewed", 32, 8, 128, 2048, 768, "zipf", 1.2),
     "dsv3": Workload("dsv3", 16384, 8, 256, 7168, 2048, "zipf", 1.0),
+    "dsv3_slice": Workload("dsv3_slice", 2048, 8, 32, 7168, 2048, "zipf", 1.0),
 }
 
 
