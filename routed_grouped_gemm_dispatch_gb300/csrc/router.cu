@@ -13,11 +13,12 @@
 //     when S > 1) from TMEM into its owners' shared memory, one slot per
 //     source CTA (distributed shared memory stores, no round trips);
 //  2. after a cluster barrier each owner sums the S slots of its tokens in
-//     rank order, one warp per token with the experts spread over the lanes
-//     (expert e in lane e % 32): a butterfly maximum, a butterfly sum of
-//     exp(l - max), and the top-k as k rounds of a butterfly arg-max
-//     (descending logit, ties to the lower expert index); lane q writes the
-//     q-th choice.
+//     rank order, T = 4*S consecutive lanes per token (expert e to lane
+//     e % T): every lane keeps a sorted list of its best KMAX logits
+//     (descending, ties to the lower expert index), built from bitonic sorts
+//     of KMAX logits at a time; the token's lanes merge their lists in
+//     butterfly rounds (a bitonic top-KMAX merge of two sorted lists), then
+//     sum exp(l - max) against the known maximum and write the top-k.
 // The top-k is decided on the logits (softmax preserves their order).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -44,7 +45,6 @@ constexpr int R_STAGE_BYTES = R_A_BYTES + R_B_MAX_BYTES;
 constexpr int R_EPI_WARPS = 16;
 constexpr int R_THREADS = 64 + 32 * R_EPI_WARPS;     // producer, MMA, epilogue warps
 constexpr int R_MAX_E = 256;                         // MOE_ROUTER_MAX_EXPERTS
-constexpr int R_VPL = R_MAX_E / 32;                  // logits per lane of a token's warp, at most
 constexpr uint64_t R_WAIT_NS = 2000000000ull;
 constexpr uint64_t R_DRAIN_NS = 200000000ull;
 constexpr int R_OFF_BARS = R_STAGES * R_STAGE_BYTES;
@@ -67,13 +67,76 @@ struct RouterParams {
     int32_t* status;
 };
 
-// (l, e) ranks above (lo, eo): a larger logit, or an equal one with a lower expert index
+// Row stride of the owners' slots for S CTAs per cluster: at least the
+// 128 / S tokens a CTA owns, and congruent to 32 / T = 8 / S modulo 32, so
+// that the 32 lanes of a warp (32 / T tokens x T experts) hit 32 banks.
+__host__ __device__ constexpr int slot_stride(int S) {
+    return R_BM / S + (((8 / S - R_BM / S) % 32) + 32) % 32;
+}
+
+// (l, e) ranks above (lo, eo): a larger logit, or an equal one with a lower
+// expert index (an empty entry is (-inf, INT_MAX))
 __device__ __forceinline__ bool ranks_above(float l, int32_t e, float lo, int32_t eo) {
     return l > lo || (l == lo && e < eo);
 }
 
-// S: CTAs per cluster (1, 2, 4 or 8); CTA r runs K blocks k_blocks*r/S .. k_blocks*(r+1)/S.
-template <int S>
+// compare-exchange: the better of entries i and l ends at i
+template <int K>
+__device__ __forceinline__ void cex(float (&v)[K], int32_t (&e)[K], int i, int l) {
+    if (ranks_above(v[l], e[l], v[i], e[i])) {
+        const float tv = v[i];
+        const int32_t te = e[i];
+        v[i] = v[l];
+        e[i] = e[l];
+        v[l] = tv;
+        e[l] = te;
+    }
+}
+
+// bitonic sort into descending order (K a power of two, fully unrolled)
+template <int K>
+__device__ __forceinline__ void bitonic_sort_desc(float (&v)[K], int32_t (&e)[K]) {
+#pragma unroll
+    for (int k = 2; k <= K; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    if ((i & k) == 0) cex<K>(v, e, i, l);
+                    else cex<K>(v, e, l, i);
+                }
+            }
+        }
+    }
+}
+
+// v <- the best K of v and w (both sorted descending), sorted descending:
+// the elementwise better of v[q] and w[K-1-q] holds the best K as a bitonic
+// sequence, which one merge network sorts
+template <int K>
+__device__ __forceinline__ void merge_topk(float (&v)[K], int32_t (&e)[K], const float (&w)[K],
+                                           const int32_t (&f)[K]) {
+#pragma unroll
+    for (int q = 0; q < K; ++q)
+        if (ranks_above(w[K - 1 - q], f[K - 1 - q], v[q], e[q])) {
+            v[q] = w[K - 1 - q];
+            e[q] = f[K - 1 - q];
+        }
+#pragma unroll
+    for (int j = K >> 1; j > 0; j >>= 1) {
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int l = i ^ j;
+            if (l > i) cex<K>(v, e, i, l);
+        }
+    }
+}
+
+// S: CTAs per cluster (1, 2, 4 or 8); CTA r runs K blocks k_blocks*r/S ..
+// k_blocks*(r+1)/S.  KMAX: the length of the top-k lists (>= top_k).
+template <int S, int KMAX>
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
               const RouterParams p) {
@@ -118,10 +181,10 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     const int32_t kb_end = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (rank + 1)) / S);
     // The owner's slots, in the stage area (free once the cluster's MMAs have
     // all completed): slot of source CTA s, expert e, owned token j at
-    // (s * n_pad + e) * RS + j; the odd row stride RS keeps a token's warp,
-    // which reads 32 consecutive experts, on 32 banks.
+    // (s * n_pad + e) * RS + j.
     constexpr int ROWS = R_BM / S;                       // tokens a CTA owns
-    constexpr int RS = ROWS + 1;
+    constexpr int RS = slot_stride(S);
+    constexpr int T = 4 * S;                             // lanes per owned token
     float* slots = reinterpret_cast<float*>(smem);
 
     if (warp == 0) {
@@ -199,6 +262,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         const uint32_t dst = (S > 1 ? mapa_shared(smem_u32(slots), static_cast<uint32_t>(owner)) : smem_u32(slots)) +
                              4u * static_cast<uint32_t>(static_cast<int>(rank) * p.n_pad * RS + (row - owner * ROWS));
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const bool token = static_cast<int64_t>(row0) + row < p.n_tokens;   // rows past the last token stay unread
         for (int32_t c0 = 8 * cpart; c0 < p.n_pad; c0 += 32) {
             uint32_t v[8];
             tmem_ld_32x32b_x8(taddr + c0, v);
@@ -206,6 +270,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t a = dst + 4u * static_cast<uint32_t>((c0 + j) * RS);
+                if (!token) continue;
                 if (S > 1) st_shared_cluster_f32(a, __uint_as_float(v[j]));
                 else slots[(c0 + j) * RS + row] = __uint_as_float(v[j]);
             }
@@ -224,75 +289,67 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         for (int r = 0; r < S; ++r)
             if ((S > 1 ? ld_shared_cluster_s32(mapa_shared(abort_addr, static_cast<uint32_t>(r))) : *abort_flag) != 0)
                 ok = false;
-        // step 2: one warp per owned token
-        for (int j = warp - 2; ok && j < ROWS; j += R_EPI_WARPS) {
-            const int64_t t = static_cast<int64_t>(row0) + static_cast<int>(rank) * ROWS + j;
-            if (t >= p.n_tokens) break;
-            float l[R_VPL];
+        // step 2: T lanes per owned token; lane j takes experts j, j + T, ...
+        const int et = tid - 64;
+        const int g = et / T;                               // owned token (all 512 / T = ROWS of them)
+        const int j = et - g * T;
+        const int64_t t = static_cast<int64_t>(row0) + static_cast<int>(rank) * ROWS + g;
+        const bool live = ok && t < p.n_tokens;
+        // the token's logit of expert e: the sum of its S partial slots in rank order
+        auto logit = [&](int32_t e) {
+            float l = 0.0f;
 #pragma unroll
-            for (int i = 0; i < R_VPL; ++i) {
-                const int32_t e = lane + 32 * i;
-                float v = -INFINITY;
-                if (e < p.n_experts) {
-                    v = 0.0f;
+            for (int s = 0; s < S; ++s) l += slots[(s * p.n_pad + e) * RS + g];
+            return l;
+        };
+        float bv[KMAX];
+        int32_t bi[KMAX];
 #pragma unroll
-                    for (int s = 0; s < S; ++s) v += slots[(s * p.n_pad + e) * RS + j];
-                }
-                l[i] = v;
+        for (int q = 0; q < KMAX; ++q) {
+            bv[q] = -INFINITY;
+            bi[q] = 0x7fffffff;
+        }
+        // pass 1: this lane's best KMAX, KMAX experts at a time
+        for (int32_t e0 = j; live && e0 < p.n_experts; e0 += KMAX * T) {
+            float cv[KMAX];
+            int32_t ci[KMAX];
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) {
+                const int32_t e = e0 + q * T;
+                cv[q] = e < p.n_experts ? logit(e) : -INFINITY;
+                ci[q] = e < p.n_experts ? e : 0x7fffffff;
             }
-            // maximum and sum of exp(l - max) over the token's experts
-            float m = l[0];
+            bitonic_sort_desc<KMAX>(cv, ci);
+            merge_topk<KMAX>(bv, bi, cv, ci);
+        }
+        // merge over the token's T lanes (both partners end with the same list)
+#pragma unroll 1
+        for (int d = 1; d < T; d <<= 1) {
+            float ov[KMAX];
+            int32_t oi[KMAX];
 #pragma unroll
-            for (int i = 1; i < R_VPL; ++i) m = fmaxf(m, l[i]);
-#pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-            float sum = 0.0f;
-#pragma unroll
-            for (int i = 0; i < R_VPL; ++i)
-                if (lane + 32 * i < p.n_experts) sum += expf(l[i] - m);
-#pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
-            sum = __shfl_sync(0xffffffffu, sum, 0);         // one value for every lane
-            // top-k: k rounds of a butterfly arg-max over (logit desc, expert asc)
-            int32_t my_id = -1;
-            float my_w = 0.0f;
-            for (int q = 0; q < p.top_k; ++q) {
-                float bv = -INFINITY;
-                int32_t be = 0x7fffffff;
-#pragma unroll
-                for (int i = 0; i < R_VPL; ++i) {
-                    const int32_t e = lane + 32 * i;
-                    if (e < p.n_experts && l[i] != -INFINITY && ranks_above(l[i], e, bv, be)) {
-                        bv = l[i];
-                        be = e;
-                    }
-                }
-#pragma unroll
-                for (int d = 16; d >= 1; d >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-                    const int32_t oe = __shfl_xor_sync(0xffffffffu, be, d);
-                    if (ranks_above(ov, oe, bv, be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                // every lane holds the winner; its own lane retires it
-                if ((be & 31) == lane) {
-#pragma unroll
-                    for (int i = 0; i < R_VPL; ++i)
-                        if (lane + 32 * i == be) l[i] = -INFINITY;
-                }
-                if (lane == q) {
-                    // no finite logit left (NaN inputs): no expert
-                    my_id = be == 0x7fffffff ? -1 : be;
-                    my_w = expf(bv - m) / sum;
-                }
+            for (int q = 0; q < KMAX; ++q) {
+                ov[q] = __shfl_xor_sync(0xffffffffu, bv[q], d);
+                oi[q] = __shfl_xor_sync(0xffffffffu, bi[q], d);
             }
-            if (lane < p.top_k) {
-                // an id in range (a finite logit was found for this rank)
-                MOE_DCHECK(my_id >= 0 && my_id < p.n_experts, p.status);
-                p.topk_ids[t * p.top_k + lane] = my_id;
-                p.topk_weights[t * p.top_k + lane] = my_w;
+            merge_topk<KMAX>(bv, bi, ov, oi);
+        }
+        // pass 2: sum of exp(l - max) over the token's experts
+        const float m = bv[0];
+        float sum = 0.0f;
+        for (int32_t e = j; live && e < p.n_experts; e += T) sum += __expf(logit(e) - m);
+#pragma unroll 1
+        for (int d = 1; d < T; d <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+        sum = __shfl_sync(0xffffffffu, sum, lane & ~(T - 1));   // the token's first lane's value for all
+        if (live && j == 0) {
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) {
+                if (q < p.top_k) {
+                    // an id in range: a finite logit ranked q-th (NaN logits never rank)
+                    MOE_DCHECK(bi[q] >= 0 && bi[q] < p.n_experts, p.status);
+                    p.topk_ids[t * p.top_k + q] = bi[q] < p.n_experts ? bi[q] : -1;
+                    p.topk_weights[t * p.top_k + q] = __expf(bv[q] - m) / sum;
+                }
             }
         }
     }
@@ -362,11 +419,22 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
         return cudaErrorInvalidValue;
     const int64_t tiles = (n_tokens + R_BM - 1) / R_BM;
     // K split: the largest power of two S <= R_MAX_SPLIT with tiles x S
-    // within the SM count and at most one CTA per 64-wide K block
+    // within the SM count, at most one CTA per 64-wide K block, and the
+    // owners' slots (S x n_pad x the slot stride, fp32) within the stage area
     int64_t split = 1;
-    while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks) split *= 2;
-    auto kernel_for = [](int64_t s) {
-        return s >= 8 ? router_kernel<8> : s == 4 ? router_kernel<4> : s == 2 ? router_kernel<2> : router_kernel<1>;
+    while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks &&
+           static_cast<int64_t>(split * 2) * p.n_pad * slot_stride(static_cast<int>(split * 2)) * 4 <= R_OFF_BARS)
+        split *= 2;
+    const int kmax = top_k <= 4 ? 4 : top_k <= 8 ? 8 : 16;
+    auto kernel_for = [kmax](int64_t sp) {
+        if (kmax == 4)
+            return sp >= 8 ? router_kernel<8, 4> : sp == 4 ? router_kernel<4, 4> : sp == 2 ? router_kernel<2, 4>
+                                                                                          : router_kernel<1, 4>;
+        if (kmax == 8)
+            return sp >= 8 ? router_kernel<8, 8> : sp == 4 ? router_kernel<4, 8> : sp == 2 ? router_kernel<2, 8>
+                                                                                          : router_kernel<1, 8>;
+        return sp >= 8 ? router_kernel<8, 16> : sp == 4 ? router_kernel<4, 16> : sp == 2 ? router_kernel<2, 16>
+                                                                                        : router_kernel<1, 16>;
     };
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -381,12 +449,12 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
     // a cluster size the device can place (clusters live inside one GPC);
     // the answer is cached per device and size
     static std::mutex mu;
-    static std::map<std::pair<int, int64_t>, bool> placeable;
+    static std::map<std::tuple<int, int, int64_t>, bool> placeable;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNoDevice;
     for (; split >= 1; split /= 2) {
         std::lock_guard<std::mutex> lock(mu);
-        const auto key = std::make_pair(dev, split);
+        const auto key = std::make_tuple(dev, kmax, split);
         auto it = placeable.find(key);
         if (it == placeable.end()) {
             cudaError_t e = cudaFuncSetAttribute(kernel_for(split), cudaFuncAttributeMaxDynamicSharedMemorySize,
