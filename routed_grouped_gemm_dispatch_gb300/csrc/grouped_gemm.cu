@@ -29,9 +29,12 @@
 //    the same rows' columns 128-255.  In phase 1 each CTA's half of B is then
 //    64 gate rows followed by the same 64 up rows, so a thread finds the gate
 //    and up values of its outputs in its own lane.
-//  * Tiles are ordered in groups of about one expert's units, slice by slice
-//    inside a group (see decode_tile), so concurrent clusters share each
-//    weight slice in L2 instead of re-reading it once per unit.
+//  * Tiles are ordered in groups of units, slice by slice inside a group, so
+//    concurrent clusters share each weight slice in L2 instead of re-reading
+//    it once per unit.  One-phase launches split each expert's units evenly
+//    into as few groups as the L2 budget allows (decode_tile_groups); the
+//    single launch, and one-phase launches whose group table does not fit in
+//    shared memory, use groups of the average units per expert (decode_tile).
 //  * Inside a CTA: warp 0 issues TMA loads (128-byte swizzled tiles; a ring of
 //    three 64 KB stages, each two adjacent 64-wide K boxes of A and of B; both
 //    CTAs' copies complete on the even CTA's "full" barrier), warp 1
@@ -83,7 +86,6 @@ constexpr int HALF_ROWS = BM / 2;                          // rows of a lone blo
 constexpr uint32_t A16_BYTES = A_BOX_BYTES / 8;            // a 16-row box of A
 constexpr uint32_t A64_BYTES = A_BOX_BYTES / 2;            // a 64-row box of A
 constexpr int64_t GROUP_A_BYTES = 64ll << 20;     // A rows a tile-order group keeps hot in L2
-constexpr int32_t UNITS_PER_EXPERT_MULT = 1;
 
 static_assert(MOE_MAX_BLOCKS <= 0x7FFF, "block indices must leave the pair bit free");
 
@@ -543,7 +545,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x,
     const bool weights_streamed = 4 * counts[1] <= 5 * counts[0];
     // Tile-order group: about one expert's units (so a weight slice is shared
     // by all of them at once), at most what the host's L2 budget allows.
-    const int32_t upe = counts[0] > 0 ? UNITS_PER_EXPERT_MULT * ((counts[1] + counts[0] - 1) / counts[0]) : 1;
+    const int32_t upe = counts[0] > 0 ? (counts[1] + counts[0] - 1) / counts[0] : 1;
     int32_t grp[2] = {p.ph[0].group < upe ? p.ph[0].group : upe, p.ph[1].group < upe ? p.ph[1].group : upe};
     if (PHASE != 3 && p.expert_groups && counts[3] > 0) grp[PHASE - 1] = counts[3];   // equal per-expert groups
     const int32_t ngroups = counts[2];

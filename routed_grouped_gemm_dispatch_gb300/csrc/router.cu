@@ -13,8 +13,9 @@
 //     when S > 1) from TMEM into its owners' shared memory, one slot per
 //     source CTA (distributed shared memory stores, no round trips);
 //  2. after a cluster barrier each owner sums the S slots of its tokens in
-//     rank order, T = 4*S consecutive lanes per token (expert e to lane
-//     e % T): every lane keeps a sorted list of its best KMAX logits
+//     rank order, T consecutive lanes per token (expert e to lane e % T; T
+//     the smaller of 4*S and n_pad / KMAX): every lane keeps a sorted list of
+//     its best KMAX logits
 //     (descending, ties to the lower expert index), built from bitonic sorts
 //     of KMAX logits at a time; the token's lanes merge their lists in
 //     butterfly rounds (a bitonic top-KMAX merge of two sorted lists), then
@@ -62,16 +63,19 @@ struct RouterParams {
     int32_t tmem_cols;     // power of two >= max(32, n_pad)
     int32_t top_k;
     int32_t k_blocks;      // hidden / 64
+    int32_t lanes;         // T: lanes per token in the top-k (a power of two, 4*S at most)
+    int32_t rs;            // slot_stride(S, T)
     int32_t* topk_ids;
     float* topk_weights;
     int32_t* status;
 };
 
-// Row stride of the owners' slots for S CTAs per cluster: at least the
-// 128 / S tokens a CTA owns, and congruent to 32 / T = 8 / S modulo 32, so
-// that the 32 lanes of a warp (32 / T tokens x T experts) hit 32 banks.
-__host__ __device__ constexpr int slot_stride(int S) {
-    return R_BM / S + (((8 / S - R_BM / S) % 32) + 32) % 32;
+// Row stride of the owners' slots for S CTAs per cluster and T lanes per
+// token: at least the 128 / S tokens a CTA owns, and congruent to 32 / T
+// modulo 32, so that the 32 lanes of a warp (32 / T tokens x T experts) hit
+// 32 banks.
+__host__ __device__ constexpr int slot_stride(int S, int T) {
+    return R_BM / S + (((32 / T - R_BM / S) % 32) + 32) % 32;
 }
 
 // (l, e) ranks above (lo, eo): a larger logit, or an equal one with a lower
@@ -183,8 +187,8 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     // all completed): slot of source CTA s, expert e, owned token j at
     // (s * n_pad + e) * RS + j.
     constexpr int ROWS = R_BM / S;                       // tokens a CTA owns
-    constexpr int RS = slot_stride(S);
-    constexpr int T = 4 * S;                             // lanes per owned token
+    const int RS = p.rs;
+    const int T = p.lanes;                               // lanes per owned token
     float* slots = reinterpret_cast<float*>(smem);
 
     if (warp == 0) {
@@ -282,7 +286,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     if (S > 1) cluster_sync_all();
     else __syncthreads();
 
-    if (warp >= 2) {
+    if (warp >= 2 && tid - 64 < ROWS * p.lanes) {        // whole warps: ROWS * T is a multiple of 32
         bool ok = true;
         const uint32_t abort_addr = smem_u32(const_cast<int*>(abort_flag));
 #pragma unroll
@@ -291,7 +295,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                 ok = false;
         // step 2: T lanes per owned token; lane j takes experts j, j + T, ...
         const int et = tid - 64;
-        const int g = et / T;                               // owned token (all 512 / T = ROWS of them)
+        const int g = et / T;                               // owned token
         const int j = et - g * T;
         const int64_t t = static_cast<int64_t>(row0) + static_cast<int>(rank) * ROWS + g;
         const bool live = ok && t < p.n_tokens;
@@ -422,10 +426,18 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
     // within the SM count, at most one CTA per 64-wide K block, and the
     // owners' slots (S x n_pad x the slot stride, fp32) within the stage area
     int64_t split = 1;
-    while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks &&
-           static_cast<int64_t>(split * 2) * p.n_pad * slot_stride(static_cast<int>(split * 2)) * 4 <= R_OFF_BARS)
-        split *= 2;
     const int kmax = top_k <= 4 ? 4 : top_k <= 8 ? 8 : 16;
+    // lanes per token: one list of kmax logits each, at most the 4*S the
+    // epilogue warps give every owned token
+    auto lanes_for = [&](int64_t sp) {
+        int t = 1;
+        while (t * 2 <= 4 * sp && t * 2 * kmax <= p.n_pad) t *= 2;
+        return t < 4 ? 4 : t;
+    };
+    while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks &&
+           static_cast<int64_t>(split * 2) * p.n_pad *
+                   slot_stride(static_cast<int>(split * 2), lanes_for(split * 2)) * 4 <= R_OFF_BARS)
+        split *= 2;
     auto kernel_for = [kmax](int64_t sp) {
         if (kmax == 4)
             return sp >= 8 ? router_kernel<8, 4> : sp == 4 ? router_kernel<4, 4> : sp == 2 ? router_kernel<2, 4>
@@ -470,6 +482,8 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
         }
         if (it->second) break;
     }
+    p.lanes = lanes_for(split);
+    p.rs = slot_stride(static_cast<int>(split), p.lanes);
     attr[0].val.clusterDim.x = static_cast<unsigned>(split);
     cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
     return cudaLaunchKernelEx(&cfg, kernel_for(split), map_x, map_w, p);
