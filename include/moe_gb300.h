@@ -188,8 +188,11 @@ moe_status_t moe_combine_routed(const uint16_t* out, int64_t total_padded_tokens
  *   topk_weights  out: [n_tokens, top_k] fp32, their softmax probabilities over
  *                 all n_experts (not renormalised over the k)
  * Limits: hidden % 128 == 0, n_experts <= MOE_ROUTER_MAX_EXPERTS, top_k <=
- * min(n_experts, MOE_ROUTER_MAX_TOPK).  One kernel launch (a tcgen05 MMA tile
- * of 128 tokens x all experts per CTA, softmax and top-k in its epilogue). */
+ * min(n_experts, MOE_ROUTER_MAX_TOPK).  One kernel launch: a tcgen05 MMA tile
+ * of 128 tokens x all experts per cluster of 1-8 CTAs (hidden split over the
+ * cluster when there are fewer tiles than SMs), softmax and top-k in its
+ * epilogue.  Every wait inside it is bounded (2 s); one that runs out sets
+ * MOE_DEV_TIMEOUT in status_dev (nullable) and leaves the outputs invalid. */
 moe_status_t moe_router_topk(const uint16_t* x_tokens, int64_t n_tokens, int32_t hidden,
                              const uint16_t* router_w, int32_t n_experts, int32_t top_k,
                              int32_t* topk_ids, float* topk_weights, int32_t* status_dev, void* stream);

@@ -6,20 +6,28 @@
 // tokens and N = n_experts rounded up to 16 (at most 256).  When there are
 // fewer tiles than SMs the tile's K (hidden) is split over the S CTAs of its
 // cluster, so that tiles x S SMs stream x instead of one per tile.  Warp 0
-// streams the CTA's K range of x and W_g with TMA (4 stages of 64-wide K),
-// warp 1 owns TMEM and issues the MMAs, warps 2-17 are the epilogue:
-//  1. CTA r of the cluster owns tokens r*128/S .. (r+1)*128/S - 1 of the
-//     tile.  Every CTA stores its fp32 logits (partial sums over its K range
-//     when S > 1) from TMEM into its owners' shared memory, one slot per
-//     source CTA (distributed shared memory stores, no round trips);
-//  2. after a cluster barrier each owner sums the S slots of its tokens in
-//     rank order, T consecutive lanes per token (expert e to lane e % T; T
-//     the smaller of 4*S and n_pad / KMAX): every lane keeps a sorted list of
-//     its best KMAX logits
-//     (descending, ties to the lower expert index), built from bitonic sorts
-//     of KMAX logits at a time; the token's lanes merge their lists in
-//     butterfly rounds (a bitonic top-KMAX merge of two sorted lists), then
-//     sum exp(l - max) against the known maximum and write the top-k.
+// streams the CTA's K range of x and W_g with TMA through a ring of as many
+// 64-wide K stages as shared memory holds (up to 12), warp 1 owns TMEM and
+// issues the MMAs, warps 2-17 are the epilogue:
+//  1. The tile's valid tokens are shared out evenly: CTA r owns tokens
+//     r*R .. r*R + R - 1 (R = the valid tokens / S, rounded up).  Every CTA
+//     writes its fp32 logits (partial sums over its K range when S > 1) from
+//     TMEM into the owners' shared memory, one row per (source CTA, token):
+//     rows for other CTAs as st.async stores that count their bytes on the
+//     owner's mbarrier, so an owner waits for exactly its own rows and no
+//     cluster-wide barrier sits between the MMAs and the top-k.
+//  2. Each owner sums the S partial rows of its tokens in rank order, T lanes
+//     per token, and selects the top-k in three steps.  (a) Every lane takes
+//     the maxima of m groups of its logits; the k-th largest of the token's
+//     T*m group maxima, theta, is at most the k-th largest logit, because k
+//     distinct logits (the group maxima) reach it.  (b) The logits >= theta
+//     are the candidates (typically k to 2k of them); the same pass sums
+//     exp(l - max) for the softmax.  (c) Each candidate's rank is the number
+//     of candidates that rank above it (a larger logit, or an equal one with
+//     a lower expert index), and a candidate of rank q < k is output q.  A
+//     token whose candidates overflow the list (many equal logits) takes the
+//     general path instead: per-lane sorted lists of the best KMAX logits
+//     (bitonic sorts), merged over the token's lanes in butterfly rounds.
 // The top-k is decided on the logits (softmax preserves their order).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -39,20 +47,23 @@ namespace {
 
 constexpr int R_BM = 128;
 constexpr int R_BK = 64;
-constexpr int R_STAGES = 4;
-constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB
-constexpr int R_B_MAX_BYTES = 256 * R_BK * 2;        // 32 KB
-constexpr int R_STAGE_BYTES = R_A_BYTES + R_B_MAX_BYTES;
+constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB of x per stage
+constexpr int R_MAX_STAGES = 12;
+constexpr int R_MIN_STAGES = 2;
 constexpr int R_EPI_WARPS = 16;
-constexpr int R_THREADS = 64 + 32 * R_EPI_WARPS;     // producer, MMA, epilogue warps
+constexpr int R_EPI_THREADS = 32 * R_EPI_WARPS;
+constexpr int R_THREADS = 64 + R_EPI_THREADS;        // producer, MMA, epilogue warps
 constexpr int R_MAX_E = 256;                         // MOE_ROUTER_MAX_EXPERTS
+constexpr int R_CMAX = 32;                           // candidate list length per token
+constexpr int R_CSTRIDE = 2 * R_CMAX + 4;            // words per token's list (16-byte rows, == 4 mod 32)
+constexpr int R_MMAX = 8;                            // group maxima per lane
 constexpr uint64_t R_WAIT_NS = 2000000000ull;
 constexpr uint64_t R_DRAIN_NS = 200000000ull;
-constexpr int R_OFF_BARS = R_STAGES * R_STAGE_BYTES;
-constexpr int R_OFF_TMEM = R_OFF_BARS + (2 * R_STAGES + 2) * 8;
-constexpr int R_OFF_ABORT = R_OFF_TMEM + 4;
-constexpr size_t R_SMEM = 1024 + R_OFF_ABORT + 16;
-constexpr int R_MAX_SPLIT = 8;   // CTAs per cluster (the portable cluster size)
+constexpr int R_MAX_SPLIT = 8;                       // CTAs per cluster (the portable cluster size)
+constexpr int R_SMEM_MAX = 227 * 1024;               // dynamic shared memory asked for at most
+constexpr int R_NUM_BARS = 2 * R_MAX_STAGES + 3;     // full, empty, tfull, drain, slots
+constexpr int R_MISC_BYTES = R_NUM_BARS * 8 + 16;    // barriers, TMEM slot, abort flag
+constexpr int R_CAND_BYTES = R_BM * R_CSTRIDE * 4;  // the lists of 128 tokens
 
 static_assert(R_MAX_E == MOE_ROUTER_MAX_EXPERTS, "router expert limit");
 
@@ -63,19 +74,58 @@ struct RouterParams {
     int32_t tmem_cols;     // power of two >= max(32, n_pad)
     int32_t top_k;
     int32_t k_blocks;      // hidden / 64
-    int32_t lanes;         // T: lanes per token in the top-k (a power of two, 4*S at most)
-    int32_t rs;            // slot_stride(S, T)
+    int32_t stages;        // ring stages (R_MIN_STAGES .. R_MAX_STAGES)
+    int32_t stage_bytes;   // 16 KB of x + n_pad rows of W_g, 64 wide
+    int32_t rs;            // floats per slot row: >= n_pad, == 4 mod 32
+    int32_t off_slots;     // byte offsets from the 1024-aligned base
+    int32_t off_cand;
+    int32_t off_bars;
     int32_t* topk_ids;
     float* topk_weights;
     int32_t* status;
 };
 
-// Row stride of the owners' slots for S CTAs per cluster and T lanes per
-// token: at least the 128 / S tokens a CTA owns, and congruent to 32 / T
-// modulo 32, so that the 32 lanes of a warp (32 / T tokens x T experts) hit
-// 32 banks.
-__host__ __device__ constexpr int slot_stride(int S, int T) {
-    return R_BM / S + (((32 / T - R_BM / S) % 32) + 32) % 32;
+// Shared-memory layout for n_pad experts, S CTAs per cluster and at most kb
+// K blocks per CTA.  The ring comes first.  With S = 1 the slots and the
+// candidate lists reuse the ring (the CTA's own MMAs are done before they are
+// written); with S > 1 other CTAs write the slots while this CTA's MMAs may
+// still run, so the slots get their own region and only the lists reuse the
+// ring.  Returns false when no layout with R_MIN_STAGES stages fits in
+// smem_max bytes.
+struct RouterLayout {
+    int stages, stage_bytes, rs, off_slots, off_cand, off_bars;
+    size_t smem;           // dynamic shared memory to request (with alignment slack)
+};
+
+__host__ __device__ constexpr int slot_stride(int n_pad) {
+    return n_pad + (((4 - n_pad) % 32) + 32) % 32;
+}
+
+bool router_layout(int n_pad, int S, int kb, int smem_max, RouterLayout* L) {
+    L->stage_bytes = R_A_BYTES + n_pad * R_BK * 2;
+    L->rs = slot_stride(n_pad);
+    const int slot_bytes = R_BM * L->rs * 4;
+    const int budget = smem_max - 1024 - R_MISC_BYTES;
+    int ring_cap = budget - (S > 1 ? slot_bytes : 0);
+    int stages = ring_cap / L->stage_bytes;
+    if (stages > R_MAX_STAGES) stages = R_MAX_STAGES;
+    if (stages > kb) stages = kb < R_MIN_STAGES ? R_MIN_STAGES : kb;
+    if (stages < R_MIN_STAGES) return false;
+    L->stages = stages;
+    int ring = stages * L->stage_bytes;
+    if (S > 1) {
+        L->off_slots = ring;
+        L->off_cand = 0;
+        if (ring < R_CAND_BYTES) return false;   // the lists must stay clear of the slots
+        ring += slot_bytes;
+    } else {
+        L->off_slots = 0;
+        L->off_cand = slot_bytes;
+        if (ring < slot_bytes + R_CAND_BYTES) ring = slot_bytes + R_CAND_BYTES;
+    }
+    L->off_bars = ring;
+    L->smem = 1024 + static_cast<size_t>(ring) + R_MISC_BYTES;
+    return L->smem <= static_cast<size_t>(smem_max);
 }
 
 // (l, e) ranks above (lo, eo): a larger logit, or an equal one with a lower
@@ -139,7 +189,8 @@ __device__ __forceinline__ void merge_topk(float (&v)[K], int32_t (&e)[K], const
 }
 
 // S: CTAs per cluster (1, 2, 4 or 8); CTA r runs K blocks k_blocks*r/S ..
-// k_blocks*(r+1)/S.  KMAX: the length of the top-k lists (>= top_k).
+// k_blocks*(r+1)/S.  KMAX: the list length of the general top-k path
+// (>= top_k).
 template <int S, int KMAX>
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
@@ -148,53 +199,65 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + R_OFF_BARS;
-    const uint32_t bar_empty = bar_full + 8 * R_STAGES;
-    const uint32_t bar_tfull = bar_empty + 8 * R_STAGES;
+    const uint32_t bar_full = sbase + static_cast<uint32_t>(p.off_bars);
+    const uint32_t bar_empty = bar_full + 8 * R_MAX_STAGES;
+    const uint32_t bar_tfull = bar_empty + 8 * R_MAX_STAGES;
     const uint32_t bar_drain = bar_tfull + 8;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + R_OFF_TMEM);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + R_OFF_ABORT);
+    const uint32_t bar_slots = bar_drain + 8;   // the owner's rows from the other CTAs have landed
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + p.off_bars + R_NUM_BARS * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_bars + R_NUM_BARS * 8 + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t b_bytes = static_cast<uint32_t>(p.n_pad) * R_BK * 2;
+    const uint32_t rank = S > 1 ? cluster_cta_rank() : 0u;
+    const int32_t row0 = static_cast<int32_t>(blockIdx.x / S) * R_BM;
+    // the tile's valid tokens, shared out evenly over the cluster's CTAs
+    const int64_t left = p.n_tokens - row0;
+    const int32_t rows_valid = left < R_BM ? static_cast<int32_t>(left) : R_BM;
+    const int32_t rows_own = (rows_valid + S - 1) / S;
+    int32_t own_n = rows_valid - static_cast<int32_t>(rank) * rows_own;
+    own_n = own_n < 0 ? 0 : (own_n > rows_own ? rows_own : own_n);
+    const int RS = p.rs;
 
     if (tid == 0) {
-        for (int s = 0; s < R_STAGES; ++s) {
+        for (int s = 0; s < p.stages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_tfull, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_slots, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        if (S > 1) {
+            // the bytes of the rows the other S - 1 CTAs store here
+            const uint32_t bytes = static_cast<uint32_t>((S - 1) * own_n * p.n_pad * 4);
+            if (bytes) mbar_arrive_expect_tx(bar_slots, bytes);
+            else mbar_arrive(bar_slots);
+        }
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_x);
         tma_prefetch_map(&map_w);
     }
     if (warp == 1) {
-        tmem_alloc(sbase + R_OFF_TMEM, static_cast<uint32_t>(p.tmem_cols));
+        tmem_alloc(sbase + static_cast<uint32_t>(p.off_bars + R_NUM_BARS * 8), static_cast<uint32_t>(p.tmem_cols));
         tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // every CTA's slot barrier is initialised before any CTA stores into it
+    // (waited for just before the stores)
+    if (S > 1) cluster_arrive_relaxed();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t rank = S > 1 ? cluster_cta_rank() : 0u;
-    const int32_t row0 = static_cast<int32_t>(blockIdx.x / S) * R_BM;
     const int32_t kb_begin = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * rank) / S);
     const int32_t kb_end = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (rank + 1)) / S);
-    // The owner's slots, in the stage area (free once the cluster's MMAs have
-    // all completed): slot of source CTA s, expert e, owned token j at
-    // (s * n_pad + e) * RS + j.
-    constexpr int ROWS = R_BM / S;                       // tokens a CTA owns
-    const int RS = p.rs;
-    const int T = p.lanes;                               // lanes per owned token
-    float* slots = reinterpret_cast<float*>(smem);
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_normal();
-            uint32_t stage = 0, phase = 0;
+            int32_t stage = 0;
+            uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
             for (int32_t kb = kb_begin; kb < kb_end; ++kb) {
@@ -203,20 +266,20 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                     break;
                 }
                 const uint32_t fb = bar_full + 8 * stage;
-                const uint32_t sa = sbase + stage * R_STAGE_BYTES;
+                const uint32_t sa = sbase + static_cast<uint32_t>(stage * p.stage_bytes);
                 mbar_arrive_expect_tx(fb, R_A_BYTES + b_bytes);
                 tma_load_2d(sa, &map_x, fb, kb * R_BK, row0, pol);
                 tma_load_2d(sa + R_A_BYTES, &map_w, fb, kb * R_BK, 0, pol);
                 ++issued;
-                if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == p.stages) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
                 volatile int never = 0;
-                const int64_t n = issued < R_STAGES ? issued : R_STAGES;
+                const int64_t n = issued < p.stages ? issued : p.stages;
                 for (int64_t i = 0; i < n; ++i) {
                     const int64_t idx = issued - 1 - i;
-                    mbar_wait_bounded(bar_full + 8 * static_cast<uint32_t>(idx % R_STAGES),
-                                      static_cast<uint32_t>((idx / R_STAGES) & 1), &never, R_DRAIN_NS);
+                    mbar_wait_bounded(bar_full + 8 * static_cast<uint32_t>(idx % p.stages),
+                                      static_cast<uint32_t>((idx / p.stages) & 1), &never, R_DRAIN_NS);
                 }
             }
         }
@@ -224,7 +287,8 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32acc(R_BM, static_cast<uint32_t>(p.n_pad));
-            uint32_t stage = 0, phase = 0;
+            int32_t stage = 0;
+            uint32_t phase = 0;
             bool ok = true;
             for (int32_t kb = kb_begin; kb < kb_end; ++kb) {
                 if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, R_WAIT_NS)) {
@@ -232,14 +296,14 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t sa = sbase + stage * R_STAGE_BYTES;
+                const uint32_t sa = sbase + static_cast<uint32_t>(stage * p.stage_bytes);
                 const uint32_t sb = sa + R_A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < R_BK / 16; ++kk)
                     tc_mma_f16(tmem_base, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32), idesc,
                                (kb != kb_begin || kk != 0) ? 1u : 0u);
                 tc_commit(bar_empty + 8 * stage);
-                if (++stage == R_STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == p.stages) { stage = 0; phase ^= 1u; }
             }
             if (ok) tc_commit(bar_tfull);
             volatile int never = 0;
@@ -251,108 +315,264 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         if (mbar_wait_bounded(bar_tfull, 0, abort_flag, R_WAIT_NS)) tc_fence_after_sync();
         __syncwarp();
     }
-    // every CTA of the cluster has finished its MMAs (its stage area is free)
-    if (S > 1) cluster_sync_all();
-    else __syncthreads();
+    if (S > 1) cluster_wait_acquire();
 
+    // ---- step 1: TMEM -> the owners' slot rows.  Warp w reads TMEM lanes
+    // 32*(w%4) .. +31 (one token each); the four warps of a lane quarter take
+    // every fourth group of 8 columns.  Slot row (source rank s, owned token
+    // g) starts at float (s * rows_own + g) * RS of the slot region.
     if (warp >= 2 && !*abort_flag) {
-        // step 1: TMEM -> the owners' slots.  Warp w reads TMEM lanes
-        // 32*(w%4) .. +31 (one token each); the four warps of a lane quarter
-        // take every fourth group of 8 columns.
         const int quarter = warp & 3;
         const int cpart = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
-        const int owner = row / ROWS;
-        const uint32_t dst = (S > 1 ? mapa_shared(smem_u32(slots), static_cast<uint32_t>(owner)) : smem_u32(slots)) +
-                             4u * static_cast<uint32_t>(static_cast<int>(rank) * p.n_pad * RS + (row - owner * ROWS));
+        const bool valid = row < rows_valid;                 // rows past the last token are not stored
+        const int owner = valid ? row / rows_own : 0;
+        const int g = row - owner * rows_own;
+        const uint32_t off = static_cast<uint32_t>(p.off_slots) +
+                             4u * static_cast<uint32_t>((static_cast<int>(rank) * rows_own + g) * RS);
+        const bool remote = S > 1 && owner != static_cast<int>(rank);
+        const uint32_t raddr = remote ? mapa_shared(sbase + off, static_cast<uint32_t>(owner)) : 0u;
+        const uint32_t rbar = remote ? mapa_shared(bar_slots, static_cast<uint32_t>(owner)) : 0u;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        const bool token = static_cast<int64_t>(row0) + row < p.n_tokens;   // rows past the last token stay unread
-        for (int32_t c0 = 8 * cpart; c0 < p.n_pad; c0 += 32) {
-            uint32_t v[8];
-            tmem_ld_32x32b_x8(taddr + c0, v);
-            tmem_ld_wait();
+        // all of the warp's column groups (at most 8: n_pad <= 256) in flight at once
+        uint32_t v[8][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t a = dst + 4u * static_cast<uint32_t>((c0 + j) * RS);
-                if (!token) continue;
-                if (S > 1) st_shared_cluster_f32(a, __uint_as_float(v[j]));
-                else slots[(c0 + j) * RS + row] = __uint_as_float(v[j]);
+        for (int i = 0; i < 8; ++i)
+            if (8 * cpart + 32 * i < p.n_pad) tmem_ld_32x32b_x8(taddr + 8 * cpart + 32 * i, v[i]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int32_t c0 = 8 * cpart + 32 * i;
+            if (!valid || c0 >= p.n_pad) continue;
+            const float f0 = __uint_as_float(v[i][0]), f1 = __uint_as_float(v[i][1]), f2 = __uint_as_float(v[i][2]),
+                        f3 = __uint_as_float(v[i][3]), f4 = __uint_as_float(v[i][4]), f5 = __uint_as_float(v[i][5]),
+                        f6 = __uint_as_float(v[i][6]), f7 = __uint_as_float(v[i][7]);
+            if (remote) {
+                st_async_v4_f32(raddr + 4u * c0, f0, f1, f2, f3, rbar);
+                st_async_v4_f32(raddr + 4u * c0 + 16u, f4, f5, f6, f7, rbar);
+            } else {
+                float4* d = reinterpret_cast<float4*>(smem + off + 4u * c0);
+                d[0] = make_float4(f0, f1, f2, f3);
+                d[1] = make_float4(f4, f5, f6, f7);
             }
         }
     }
-    // every slot is written (and every CTA's abort flag is final)
     tc_fence_before_sync();
     __syncwarp();
-    if (S > 1) cluster_sync_all();
-    else __syncthreads();
+    if (warp >= 2) named_bar_sync(1, R_EPI_THREADS);        // this CTA's own rows are in place
+    // waited for at the end: no CTA exits while another may still store into it
+    if (S > 1) cluster_arrive_relaxed();
 
-    if (warp >= 2 && tid - 64 < ROWS * p.lanes) {        // whole warps: ROWS * T is a multiple of 32
-        bool ok = true;
-        const uint32_t abort_addr = smem_u32(const_cast<int*>(abort_flag));
-#pragma unroll
-        for (int r = 0; r < S; ++r)
-            if ((S > 1 ? ld_shared_cluster_s32(mapa_shared(abort_addr, static_cast<uint32_t>(r))) : *abort_flag) != 0)
-                ok = false;
-        // step 2: T lanes per owned token; lane j takes experts j, j + T, ...
+    // ---- step 2: the top-k of each owned token, T lanes per token
+    if (warp >= 2) {
+        bool ok = !*abort_flag;
+        if (S > 1 && own_n > 0 && ok) ok = mbar_wait_bounded<true>(bar_slots, 0, abort_flag, R_WAIT_NS);
+        ok = __all_sync(0xffffffffu, ok);
+        // lanes per token: a power of two, 4..32, whose chunks of 4 tile the
+        // n_pad columns exactly
+        int T = 32;
+        while (T > 4 && (p.n_pad % (4 * T) != 0 || T * rows_own > R_EPI_THREADS)) T >>= 1;
         const int et = tid - 64;
-        const int g = et / T;                               // owned token
-        const int j = et - g * T;
-        const int64_t t = static_cast<int64_t>(row0) + static_cast<int>(rank) * ROWS + g;
-        const bool live = ok && t < p.n_tokens;
-        // the token's logit of expert e: the sum of its S partial slots in rank order
-        auto logit = [&](int32_t e) {
-            float l = 0.0f;
+        const int g = et / T;                                 // owned token
+        const int j = et & (T - 1);                           // lane within the token
+        if (ok && (et & ~31) / T < own_n) {                   // warp-uniform: the warp has a live token
+            const bool live = g < own_n;
+            const int64_t t = static_cast<int64_t>(row0) + static_cast<int>(rank) * rows_own + g;
+            const int nq = p.n_pad / (4 * T);                 // float4 chunks per lane
+            int m = 1;                                        // group maxima per lane
+            while (m < R_MMAX && T * m < 2 * p.top_k && nq % (2 * m) == 0) m <<= 1;
+            const int qpg = nq / m;                           // chunks per group
+            const int ng = T * m;                             // group maxima per token
+            const float* row_s0 = reinterpret_cast<const float*>(smem + p.off_slots) + g * RS;
+            const int sstride = rows_own * RS;                // floats between two source ranks' rows
+            // chunk q of this lane: experts 4(j + qT) .. +3, the S partial rows summed in rank order
+            auto chunk = [&](int q) {
+                const int c = 4 * (j + q * T);
+                float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-            for (int s = 0; s < S; ++s) l += slots[(s * p.n_pad + e) * RS + g];
-            return l;
-        };
-        float bv[KMAX];
-        int32_t bi[KMAX];
+                for (int s = 0; s < S; ++s) {
+                    const float4 b = *reinterpret_cast<const float4*>(row_s0 + s * sstride + c);
+                    a.x += b.x;
+                    a.y += b.y;
+                    a.z += b.z;
+                    a.w += b.w;
+                }
+                return a;
+            };
+            auto logit = [&](int32_t e) {
+                float l = 0.0f;
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) {
-            bv[q] = -INFINITY;
-            bi[q] = 0x7fffffff;
-        }
-        // pass 1: this lane's best KMAX, KMAX experts at a time
-        for (int32_t e0 = j; live && e0 < p.n_experts; e0 += KMAX * T) {
-            float cv[KMAX];
-            int32_t ci[KMAX];
+                for (int s = 0; s < S; ++s) l += row_s0[s * sstride + e];
+                return l;
+            };
+            float* list = reinterpret_cast<float*>(smem + p.off_cand) + g * R_CSTRIDE;   // (logit, expert) pairs
+            const int n_e = p.n_experts;
+            // A lane whose logits fit one list (at most KMAX) in a token of at
+            // most 8 lanes (three merge rounds) takes the list path directly;
+            // every other token selects through theta first.
+            const bool direct = 4 * nq <= KMAX && T <= 8;
+            float mx = -INFINITY, sum = 0.0f;                 // the token's max logit and sum of exp(l - mx)
+            bool general = true;
+            if (!direct) {
+                // (a) group maxima (padding experts count as -inf; NaN never wins
+                // a max), kept in registers and in the list for the token's lanes
+                float gm[R_MMAX];
 #pragma unroll
-            for (int q = 0; q < KMAX; ++q) {
-                const int32_t e = e0 + q * T;
-                cv[q] = e < p.n_experts ? logit(e) : -INFINITY;
-                ci[q] = e < p.n_experts ? e : 0x7fffffff;
+                for (int a = 0; a < R_MMAX; ++a) gm[a] = -INFINITY;
+                if (live) {
+#pragma unroll
+                    for (int a = 0; a < R_MMAX; ++a) {
+                        if (a >= m) break;
+                        for (int qq = 0; qq < qpg; ++qq) {
+                            const int q = a * qpg + qq;
+                            const float4 v = chunk(q);
+                            const int e0 = 4 * (j + q * T);
+                            gm[a] = fmaxf(gm[a], e0 < n_e ? v.x : -INFINITY);
+                            gm[a] = fmaxf(gm[a], e0 + 1 < n_e ? v.y : -INFINITY);
+                            gm[a] = fmaxf(gm[a], e0 + 2 < n_e ? v.z : -INFINITY);
+                            gm[a] = fmaxf(gm[a], e0 + 3 < n_e ? v.w : -INFINITY);
+                        }
+                        list[j * m + a] = gm[a];
+                    }
+                }
+                float th = INFINITY;
+#pragma unroll
+                for (int a = 0; a < R_MMAX; ++a) mx = fmaxf(mx, gm[a]);
+                __syncwarp();
+                // theta: the k-th largest of the token's ng <= 32 group maxima
+                // (the smallest of them with fewer than k others above it)
+                if (live) {
+                    float4 all[8];
+#pragma unroll
+                    for (int i4 = 0; i4 < 8; ++i4)
+                        all[i4] = 4 * i4 < ng ? reinterpret_cast<const float4*>(list)[i4]
+                                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+                    for (int a = 0; a < R_MMAX; ++a) {
+                        if (a >= m) break;
+                        int above = 0;
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4)
+                            above += (all[i4].x > gm[a] ? 1 : 0) + (all[i4].y > gm[a] ? 1 : 0) +
+                                     (all[i4].z > gm[a] ? 1 : 0) + (all[i4].w > gm[a] ? 1 : 0);
+                        if (above < p.top_k) th = fminf(th, gm[a]);
+                    }
+                }
+                for (int d = 1; d < T; d <<= 1) {
+                    th = fminf(th, __shfl_xor_sync(0xffffffffu, th, d));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+                }
+                __syncwarp();                                     // the maxima are read: the list is free
+                // (b) candidates (logit >= theta): a bit per value of this lane,
+                // then one prefix sum over the token's lanes places them in the
+                // list; the same pass sums exp(l - max)
+                uint64_t cbits = 0;                               // bit 4q + i: value i of chunk q (V <= 64)
+                if (live) {
+                    for (int q = 0; q < nq; ++q) {
+                        const float4 v4 = chunk(q);
+                        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if (4 * (j + q * T) + i >= n_e) continue;
+                            sum += __expf(vv[i] - mx);
+                            if (vv[i] >= th) cbits |= 1ull << (4 * q + i);
+                        }
+                    }
+                }
+                const int mine = __popcll(cbits);
+                int incl = mine;                                  // inclusive prefix over the token's lanes
+                for (int d = 1; d < T; d <<= 1) {
+                    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (j >= d) incl += o;
+                    sum += __shfl_xor_sync(0xffffffffu, sum, d);
+                }
+                const int c = __shfl_sync(0xffffffffu, incl, (lane & ~(T - 1)) + T - 1);   // the token's candidates
+                for (int pos = incl - mine; cbits != 0 && pos < R_CMAX; ++pos) {
+                    const int li = __ffsll(static_cast<long long>(cbits)) - 1;
+                    cbits &= cbits - 1;
+                    const int e = 4 * (j + (li >> 2) * T) + (li & 3);
+                    reinterpret_cast<float2*>(list)[pos] = make_float2(logit(e), __int_as_float(e));
+                }
+                __syncwarp();
+                general = __any_sync(0xffffffffu, live && (c > R_CMAX || ng < p.top_k));
+                if (!general) {
+                    // (c) rank the candidates: the k best are exactly those of rank < k
+                    if (live) {
+                        const float2* cl = reinterpret_cast<const float2*>(list);
+                        const float inv = 1.0f / sum;
+                        for (int i = j; i < c; i += T) {
+                            const float2 me = cl[i];
+                            const int32_t ei = __float_as_int(me.y);
+                            int r = 0;
+#pragma unroll 4
+                            for (int i2 = 0; i2 < c; ++i2) {
+                                const float2 o = cl[i2];
+                                r += ranks_above(o.x, __float_as_int(o.y), me.x, ei) ? 1 : 0;
+                            }
+                            if (r < p.top_k) {
+                                MOE_DCHECK(ei >= 0 && ei < n_e, p.status);
+                                p.topk_ids[t * p.top_k + r] = ei;
+                                p.topk_weights[t * p.top_k + r] = __expf(me.x - mx) * inv;
+                            }
+                        }
+                        // fewer candidates than k (NaN logits never rank): empty outputs
+                        for (int r = c + j; r < p.top_k; r += T) {
+                            p.topk_ids[t * p.top_k + r] = -1;
+                            p.topk_weights[t * p.top_k + r] = 0.0f;
+                        }
+                    }
+                }
             }
-            bitonic_sort_desc<KMAX>(cv, ci);
-            merge_topk<KMAX>(bv, bi, cv, ci);
-        }
-        // merge over the token's T lanes (both partners end with the same list)
-#pragma unroll 1
-        for (int d = 1; d < T; d <<= 1) {
-            float ov[KMAX];
-            int32_t oi[KMAX];
+            if (general) {
+                // general path: lane j keeps a sorted list of its best KMAX of
+                // experts j, j + T, ..., built KMAX at a time with bitonic
+                // sorts; the token's lanes merge their lists in butterfly rounds
+                float bv[KMAX];
+                int32_t bi[KMAX];
 #pragma unroll
-            for (int q = 0; q < KMAX; ++q) {
-                ov[q] = __shfl_xor_sync(0xffffffffu, bv[q], d);
-                oi[q] = __shfl_xor_sync(0xffffffffu, bi[q], d);
-            }
-            merge_topk<KMAX>(bv, bi, ov, oi);
-        }
-        // pass 2: sum of exp(l - max) over the token's experts
-        const float m = bv[0];
-        float sum = 0.0f;
-        for (int32_t e = j; live && e < p.n_experts; e += T) sum += __expf(logit(e) - m);
-#pragma unroll 1
-        for (int d = 1; d < T; d <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
-        sum = __shfl_sync(0xffffffffu, sum, lane & ~(T - 1));   // the token's first lane's value for all
-        if (live && j == 0) {
+                for (int q = 0; q < KMAX; ++q) {
+                    bv[q] = -INFINITY;
+                    bi[q] = 0x7fffffff;
+                }
+                for (int32_t e0 = j; live && e0 < n_e; e0 += KMAX * T) {
+                    float cv[KMAX];
+                    int32_t ci[KMAX];
 #pragma unroll
-            for (int q = 0; q < KMAX; ++q) {
-                if (q < p.top_k) {
-                    // an id in range: a finite logit ranked q-th (NaN logits never rank)
-                    MOE_DCHECK(bi[q] >= 0 && bi[q] < p.n_experts, p.status);
-                    p.topk_ids[t * p.top_k + q] = bi[q] < p.n_experts ? bi[q] : -1;
-                    p.topk_weights[t * p.top_k + q] = __expf(bv[q] - m) / sum;
+                    for (int q = 0; q < KMAX; ++q) {
+                        const int32_t e = e0 + q * T;
+                        cv[q] = e < n_e ? logit(e) : -INFINITY;
+                        ci[q] = e < n_e ? e : 0x7fffffff;
+                    }
+                    bitonic_sort_desc<KMAX>(cv, ci);
+                    merge_topk<KMAX>(bv, bi, cv, ci);
+                }
+#pragma unroll 1
+                for (int d = 1; d < T; d <<= 1) {
+                    float ov[KMAX];
+                    int32_t oi[KMAX];
+#pragma unroll
+                    for (int q = 0; q < KMAX; ++q) {
+                        ov[q] = __shfl_xor_sync(0xffffffffu, bv[q], d);
+                        oi[q] = __shfl_xor_sync(0xffffffffu, bi[q], d);
+                    }
+                    merge_topk<KMAX>(bv, bi, ov, oi);
+                }
+                if (direct) {
+                    // the merged list is the same in all of the token's lanes
+                    mx = bv[0];
+                    for (int32_t e = j; live && e < n_e; e += T) sum += __expf(logit(e) - mx);
+                    for (int d = 1; d < T; d <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+                }
+                if (live && j == 0) {
+#pragma unroll
+                    for (int q = 0; q < KMAX; ++q) {
+                        if (q < p.top_k) {
+                            // an id in range: a finite logit ranked q-th (NaN logits never rank)
+                            MOE_DCHECK(bi[q] >= 0 && bi[q] < n_e, p.status);
+                            p.topk_ids[t * p.top_k + q] = bi[q] < n_e ? bi[q] : -1;
+                            p.topk_weights[t * p.top_k + q] = bi[q] < n_e ? __expf(bv[q] - mx) / sum : 0.0f;
+                        }
+                    }
                 }
             }
         }
@@ -360,6 +580,7 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
 
     tc_fence_before_sync();
     __syncthreads();
+    if (S > 1) cluster_wait_acquire();
     if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
     if (warp == 1) {
         tc_fence_after_sync();
@@ -423,21 +644,23 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
         return cudaErrorInvalidValue;
     const int64_t tiles = (n_tokens + R_BM - 1) / R_BM;
     // K split: the largest power of two S <= R_MAX_SPLIT with tiles x S
-    // within the SM count, at most one CTA per 64-wide K block, and the
-    // owners' slots (S x n_pad x the slot stride, fp32) within the stage area
-    int64_t split = 1;
-    const int kmax = top_k <= 4 ? 4 : top_k <= 8 ? 8 : 16;
-    // lanes per token: one list of kmax logits each, at most the 4*S the
-    // epilogue warps give every owned token
-    auto lanes_for = [&](int64_t sp) {
-        int t = 1;
-        while (t * 2 <= 4 * sp && t * 2 * kmax <= p.n_pad) t *= 2;
-        return t < 4 ? 4 : t;
+    // within the SM count, at most one CTA per 64-wide K block, and a
+    // shared-memory layout that fits
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return cudaErrorNoDevice;
+    const int smem_max = optin < R_SMEM_MAX ? optin : R_SMEM_MAX;
+    auto layout_for = [&](int64_t sp, RouterLayout* L) {
+        const int kb = static_cast<int>((p.k_blocks + sp - 1) / sp);
+        return router_layout(p.n_pad, static_cast<int>(sp), kb, smem_max, L);
     };
+    RouterLayout L{};
+    int64_t split = 1;
     while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks &&
-           static_cast<int64_t>(split * 2) * p.n_pad *
-                   slot_stride(static_cast<int>(split * 2), lanes_for(split * 2)) * 4 <= R_OFF_BARS)
+           layout_for(split * 2, &L))
         split *= 2;
+    const int kmax = top_k <= 4 ? 4 : top_k <= 8 ? 8 : 16;
     auto kernel_for = [kmax](int64_t sp) {
         if (kmax == 4)
             return sp >= 8 ? router_kernel<8, 4> : sp == 4 ? router_kernel<4, 4> : sp == 2 ? router_kernel<2, 4>
@@ -454,26 +677,28 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg{};
     cfg.blockDim = dim3(R_THREADS);
-    cfg.dynamicSmemBytes = R_SMEM;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // a cluster size the device can place (clusters live inside one GPC);
-    // the answer is cached per device and size
+    // the answer is cached per device, kernel and shared-memory size
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int64_t>, bool> placeable;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNoDevice;
+    static std::map<std::tuple<int, int, int64_t, size_t>, bool> placeable;
     for (; split >= 1; split /= 2) {
+        if (!layout_for(split, &L)) {
+            if (split == 1) return cudaErrorInvalidConfiguration;
+            continue;
+        }
         std::lock_guard<std::mutex> lock(mu);
-        const auto key = std::make_tuple(dev, kmax, split);
+        const auto key = std::make_tuple(dev, kmax, split, L.smem);
         auto it = placeable.find(key);
         if (it == placeable.end()) {
             cudaError_t e = cudaFuncSetAttribute(kernel_for(split), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(R_SMEM));
+                                                 smem_max);
             if (e != cudaSuccess) return e;
             attr[0].val.clusterDim.x = static_cast<unsigned>(split);
             cfg.gridDim = dim3(static_cast<unsigned>(split));
+            cfg.dynamicSmemBytes = L.smem;
             int n = 0;
             const bool ok = split == 1 || (cudaOccupancyMaxActiveClusters(&n, kernel_for(split), &cfg) == cudaSuccess &&
                                            n > 0);
@@ -482,10 +707,15 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
         }
         if (it->second) break;
     }
-    p.lanes = lanes_for(split);
-    p.rs = slot_stride(static_cast<int>(split), p.lanes);
+    p.stages = L.stages;
+    p.stage_bytes = L.stage_bytes;
+    p.rs = L.rs;
+    p.off_slots = L.off_slots;
+    p.off_cand = L.off_cand;
+    p.off_bars = L.off_bars;
     attr[0].val.clusterDim.x = static_cast<unsigned>(split);
     cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
+    cfg.dynamicSmemBytes = L.smem;
     return cudaLaunchKernelEx(&cfg, kernel_for(split), map_x, map_w, p);
 }
 

@@ -42,23 +42,39 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t cta_rank
     return r;
 }
 
-// Load a 32-bit value from the shared memory of a CTA of this cluster, given
-// its shared::cluster address (see mapa_shared).
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-    return v;
+// Store four floats into the shared memory of another CTA of this cluster
+// (shared::cluster addresses, see mapa_shared) and count their 16 bytes as
+// complete_tx on that CTA's mbarrier `cluster_bar`.  The store is weak; the
+// complete_tx has release semantics at cluster scope, so a thread that sees
+// the barrier's phase complete with an acquire.cluster wait sees the data.
+__device__ __forceinline__ void st_async_v4_f32(uint32_t cluster_addr, float a, float b, float c, float d,
+                                                uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+                 : "memory");
 }
 
-__device__ __forceinline__ int32_t ld_shared_cluster_s32(uint32_t cluster_addr) {
-    int32_t v;
-    asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
+// The two halves of a cluster barrier: every thread of every CTA of the
+// cluster arrives once per phase and waits once per phase, in that order.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
-// Store a 32-bit value into the shared memory of a CTA of this cluster.
-__device__ __forceinline__ void st_shared_cluster_f32(uint32_t cluster_addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+// An arrive that orders nothing (the arrive does not wait for this thread's
+// earlier memory operations).  Mbarrier initialisation is published by
+// fence_mbar_init before it.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Barrier among `nthreads` threads (whole warps) of the CTA on hardware
+// barrier `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Every thread of every CTA in the cluster arrives, then waits for all.
@@ -100,18 +116,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, with acquire semantics at cluster scope (for phases
+// completed by other CTAs' st.async / remote arrives).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete, for at most
 // `limit_ns` nanoseconds.  Gives up early when *abort becomes non-zero (another
 // role of the CTA ran out of time).  Returns false when it gave up; on a
-// timeout it raises *abort itself so the rest of the CTA stops too.
+// timeout it raises *abort itself so the rest of the CTA stops too.  kCluster:
+// acquire at cluster scope (phases completed from other CTAs).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort = 1;

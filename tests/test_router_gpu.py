@@ -76,3 +76,30 @@ def test_router_host_validation():
         moe.router_topk(x, torch.zeros((300, 128), dtype=torch.float16, device="cuda"), 2)
     with pytest.raises(moe.MoeError):
         moe.router_topk(x, torch.zeros((8, 128), dtype=torch.float16, device="cuda"), 9)
+
+
+def _exact_case(T, E, H, seed, zero_w=False):
+    """Inputs whose fp32 logits are exact integers (entries in {-1, 0, 1}), so
+    that every summation order gives the same logits and equal logits are
+    exact ties: the chosen experts, ties to the lower index, must be the
+    oracle's exactly."""
+    rng = np.random.default_rng(seed)
+    x = rng.integers(-1, 2, size=(T, H)).astype(np.float16)
+    wg = np.zeros((E, H), np.float16) if zero_w else rng.integers(-1, 2, size=(E, H)).astype(np.float16)
+    return x, wg
+
+
+@pytest.mark.parametrize("T,E,k,H,zero_w", [
+    (300, 64, 6, 128, False), (200, 256, 8, 256, False), (130, 16, 16, 128, False), (64, 40, 5, 128, False),
+    (33, 128, 8, 2048, False),                       # one ragged tile, the hidden split over the cluster
+    (100, 64, 6, 128, True), (100, 256, 8, 128, True), (100, 16, 4, 128, True), (20, 128, 8, 1024, True)])
+def test_router_exact_ties(T, E, k, H, zero_w):
+    x, wg = _exact_case(T, E, H, seed=T + E, zero_w=zero_w)
+    ids_o, w_o = oracle.router(x, wg, k)
+    ids_g, w_g = moe.router_topk(torch.from_numpy(x).cuda(), torch.from_numpy(wg).cuda(), k)
+    torch.cuda.synchronize()
+    ids_g, w_g = ids_g.cpu().numpy(), w_g.cpu().numpy()
+    assert np.array_equal(ids_g, ids_o)
+    assert np.allclose(w_g, w_o, rtol=2e-5, atol=1e-8)
+    if zero_w:
+        assert np.array_equal(ids_g, np.broadcast_to(np.arange(k, dtype=np.int32), (T, k)))
