@@ -6,8 +6,8 @@
 // tokens and N = n_experts rounded up to 16 (at most 256).  When there are
 // fewer tiles than SMs the tile's K (hidden) is split over the S CTAs of its
 // cluster, so that tiles x S SMs stream x instead of one per tile.  Warp 0
-// streams the CTA's K range of x and W_g with TMA through a ring of as many
-// 64-wide K stages as shared memory holds (up to 12), warp 1 owns TMEM and
+// streams the CTA's K range of x and W_g with TMA through a ring of up to
+// four 64-wide K stages (fewer when the slots leave no room), warp 1 owns TMEM and
 // issues the MMAs, warps 2-17 are the epilogue:
 //  1. The tile's valid tokens are shared out evenly: CTA r owns tokens
 //     r*R .. r*R + R - 1 (R = the valid tokens / S, rounded up).  Every CTA
@@ -48,7 +48,7 @@ namespace {
 constexpr int R_BM = 128;
 constexpr int R_BK = 64;
 constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB of x per stage
-constexpr int R_MAX_STAGES = 12;
+constexpr int R_MAX_STAGES = 4;                  // deeper rings measured no faster
 constexpr int R_MIN_STAGES = 2;
 constexpr int R_EPI_WARPS = 16;
 constexpr int R_EPI_THREADS = 32 * R_EPI_WARPS;
