@@ -7,8 +7,11 @@
 // fewer tiles than SMs the tile's K (hidden) is split over the S CTAs of its
 // cluster, so that tiles x S SMs stream x instead of one per tile.  Warp 0
 // streams the CTA's K range of x and W_g with TMA through a ring of up to
-// four 64-wide K stages (fewer when the slots leave no room), warp 1 owns TMEM and
-// issues the MMAs, warps 2-17 are the epilogue:
+// eight 64-wide K stages (as many as shared memory holds beside the slots),
+// warp 1 owns TMEM and issues the MMAs, warps 2-17 are the epilogue.  With
+// as many tiles as SMs or more there is no K split; tiles then pair up on
+// 2-SM MMAs (M = 256) in which each CTA holds its own tile's x and half of
+// W_g's rows, so each SM receives a third fewer bytes.  The epilogue:
 //  1. The tile's valid tokens are shared out evenly: CTA r owns tokens
 //     r*R .. r*R + R - 1 (R = the valid tokens / S, rounded up).  Every CTA
 //     writes its fp32 logits (partial sums over its K range when S > 1) from
@@ -48,7 +51,7 @@ namespace {
 constexpr int R_BM = 128;
 constexpr int R_BK = 64;
 constexpr int R_A_BYTES = R_BM * R_BK * 2;           // 16 KB of x per stage
-constexpr int R_MAX_STAGES = 4;                  // deeper rings measured no faster
+constexpr int R_MAX_STAGES = 8;
 constexpr int R_MIN_STAGES = 2;
 constexpr int R_EPI_WARPS = 16;
 constexpr int R_EPI_THREADS = 32 * R_EPI_WARPS;
@@ -85,8 +88,8 @@ struct RouterParams {
     int32_t* status;
 };
 
-// Shared-memory layout for n_pad experts, S CTAs per cluster and at most kb
-// K blocks per CTA.  The ring comes first.  With S = 1 the slots and the
+// Shared-memory layout for n_pad experts, S CTAs per cluster (or a pair that
+// splits W_g's rows) and at most kb K blocks per CTA.  The ring comes first.  With S = 1 the slots and the
 // candidate lists reuse the ring (the CTA's own MMAs are done before they are
 // written); with S > 1 other CTAs write the slots while this CTA's MMAs may
 // still run, so the slots get their own region and only the lists reuse the
@@ -101,8 +104,8 @@ __host__ __device__ constexpr int slot_stride(int n_pad) {
     return n_pad + (((4 - n_pad) % 32) + 32) % 32;
 }
 
-bool router_layout(int n_pad, int S, int kb, int smem_max, RouterLayout* L) {
-    L->stage_bytes = R_A_BYTES + n_pad * R_BK * 2;
+bool router_layout(int n_pad, int S, bool pair, int kb, int smem_max, RouterLayout* L) {
+    L->stage_bytes = R_A_BYTES + (pair ? n_pad / 2 : n_pad) * R_BK * 2;
     L->rs = slot_stride(n_pad);
     const int slot_bytes = R_BM * L->rs * 4;
     const int budget = smem_max - 1024 - R_MISC_BYTES;
@@ -190,8 +193,10 @@ __device__ __forceinline__ void merge_topk(float (&v)[K], int32_t (&e)[K], const
 
 // S: CTAs per cluster (1, 2, 4 or 8); CTA r runs K blocks k_blocks*r/S ..
 // k_blocks*(r+1)/S.  KMAX: the list length of the general top-k path
-// (>= top_k).
-template <int S, int KMAX>
+// (>= top_k).  PAIR (with S = 1): clusters of two CTAs, each with its own
+// tile, share one 2-SM MMA of M = 256 tokens: each CTA loads its tile's x
+// and half of W_g's rows, so each SM receives a third fewer bytes.
+template <int S, int KMAX, bool PAIR>
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
               const RouterParams p) {
@@ -207,12 +212,15 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + p.off_bars + R_NUM_BARS * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_bars + R_NUM_BARS * 8 + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t b_bytes = static_cast<uint32_t>(p.n_pad) * R_BK * 2;
-    const uint32_t rank = S > 1 ? cluster_cta_rank() : 0u;
+    const uint32_t b_bytes = static_cast<uint32_t>(PAIR ? p.n_pad / 2 : p.n_pad) * R_BK * 2;   // W_g rows per stage
+    static_assert(!PAIR || S == 1, "a pair splits W_g, not K");
+    const uint32_t rank = S > 1 ? cluster_cta_rank() : 0u;          // K-split rank
+    const uint32_t prank = PAIR ? cluster_cta_rank() : 0u;         // rank in the pair
+    const bool leader = prank == 0;
     const int32_t row0 = static_cast<int32_t>(blockIdx.x / S) * R_BM;
     // the tile's valid tokens, shared out evenly over the cluster's CTAs
-    const int64_t left = p.n_tokens - row0;
-    const int32_t rows_valid = left < R_BM ? static_cast<int32_t>(left) : R_BM;
+    const int64_t left = p.n_tokens - row0;                       // <= 0: a pair's spare CTA
+    const int32_t rows_valid = left < 0 ? 0 : (left < R_BM ? static_cast<int32_t>(left) : R_BM);
     const int32_t rows_own = (rows_valid + S - 1) / S;
     int32_t own_n = rows_valid - static_cast<int32_t>(rank) * rows_own;
     own_n = own_n < 0 ? 0 : (own_n > rows_own ? rows_own : own_n);
@@ -240,8 +248,14 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
         tma_prefetch_map(&map_w);
     }
     if (warp == 1) {
-        tmem_alloc(sbase + static_cast<uint32_t>(p.off_bars + R_NUM_BARS * 8), static_cast<uint32_t>(p.tmem_cols));
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(sbase + static_cast<uint32_t>(p.off_bars + R_NUM_BARS * 8),
+                            static_cast<uint32_t>(p.tmem_cols));
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(sbase + static_cast<uint32_t>(p.off_bars + R_NUM_BARS * 8), static_cast<uint32_t>(p.tmem_cols));
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -249,6 +263,9 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     // every CTA's slot barrier is initialised before any CTA stores into it
     // (waited for just before the stores)
     if (S > 1) cluster_arrive_relaxed();
+    // a pair: both CTAs' barriers exist before the odd CTA's copies or the
+    // leader's commits reach them
+    if (PAIR) cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     const int32_t kb_begin = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * rank) / S);
     const int32_t kb_end = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (rank + 1)) / S);
@@ -265,15 +282,24 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                     ok = false;
                     break;
                 }
-                const uint32_t fb = bar_full + 8 * stage;
                 const uint32_t sa = sbase + static_cast<uint32_t>(stage * p.stage_bytes);
-                mbar_arrive_expect_tx(fb, R_A_BYTES + b_bytes);
-                tma_load_2d(sa, &map_x, fb, kb * R_BK, row0, pol);
-                tma_load_2d(sa + R_A_BYTES, &map_w, fb, kb * R_BK, 0, pol);
+                if (PAIR) {
+                    // both CTAs' copies complete on the leader's barrier
+                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (R_A_BYTES + b_bytes));
+                    tma_load_2d_pair(sa, &map_x, fb, kb * R_BK, row0, pol);
+                    tma_load_2d_pair(sa + R_A_BYTES, &map_w, fb, kb * R_BK,
+                                     static_cast<int32_t>(prank) * (p.n_pad / 2), pol);
+                } else {
+                    const uint32_t fb = bar_full + 8 * stage;
+                    mbar_arrive_expect_tx(fb, R_A_BYTES + b_bytes);
+                    tma_load_2d(sa, &map_x, fb, kb * R_BK, row0, pol);
+                    tma_load_2d(sa + R_A_BYTES, &map_w, fb, kb * R_BK, 0, pol);
+                }
                 ++issued;
                 if (++stage == p.stages) { stage = 0; phase ^= 1u; }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 volatile int never = 0;
                 const int64_t n = issued < p.stages ? issued : p.stages;
                 for (int64_t i = 0; i < n; ++i) {
@@ -281,12 +307,17 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                     mbar_wait_bounded(bar_full + 8 * static_cast<uint32_t>(idx % p.stages),
                                       static_cast<uint32_t>((idx / p.stages) & 1), &never, R_DRAIN_NS);
                 }
+            } else if (!ok) {
+                // the odd CTA's copies report to the leader's barriers: give
+                // them a bounded moment to land
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 1000000ull) { }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32acc(R_BM, static_cast<uint32_t>(p.n_pad));
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_f16_f32acc(PAIR ? 2 * R_BM : R_BM, static_cast<uint32_t>(p.n_pad));
             int32_t stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -299,15 +330,24 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
                 const uint32_t sa = sbase + static_cast<uint32_t>(stage * p.stage_bytes);
                 const uint32_t sb = sa + R_A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < R_BK / 16; ++kk)
-                    tc_mma_f16(tmem_base, smem_desc_k_sw128(sa + kk * 32), smem_desc_k_sw128(sb + kk * 32), idesc,
-                               (kb != kb_begin || kk != 0) ? 1u : 0u);
-                tc_commit(bar_empty + 8 * stage);
+                for (int kk = 0; kk < R_BK / 16; ++kk) {
+                    const uint64_t ad = smem_desc_k_sw128(sa + kk * 32), bd = smem_desc_k_sw128(sb + kk * 32);
+                    const uint32_t acc = (kb != kb_begin || kk != 0) ? 1u : 0u;
+                    if (PAIR) tc_mma_f16_pair(tmem_base, ad, bd, idesc, acc);
+                    else tc_mma_f16(tmem_base, ad, bd, idesc, acc);
+                }
+                // the stage may be refilled (in both CTAs of a pair) once these MMAs are done
+                if (PAIR) tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+                else tc_commit(bar_empty + 8 * stage);
                 if (++stage == p.stages) { stage = 0; phase ^= 1u; }
             }
-            if (ok) tc_commit(bar_tfull);
+            if (ok) {
+                if (PAIR) tc_commit_pair_mc(bar_tfull, 0x3);
+                else tc_commit(bar_tfull);
+            }
             volatile int never = 0;
-            tc_commit(bar_drain);
+            if (PAIR) tc_commit_pair(bar_drain);
+            else tc_commit(bar_drain);
             mbar_wait_bounded(bar_drain, 0, &never, R_DRAIN_NS);
         }
         __syncwarp();
@@ -581,10 +621,14 @@ router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__
     tc_fence_before_sync();
     __syncthreads();
     if (S > 1) cluster_wait_acquire();
+    // a pair: neither CTA frees the pair's TMEM or leaves while the other may
+    // still use it or its shared memory
+    if (PAIR) cluster_sync_all();
     if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, MOE_DEV_TIMEOUT);
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+        if (PAIR) tmem_dealloc_pair(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+        else tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
     }
 }
 
@@ -643,33 +687,35 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
                     static_cast<uint32_t>(p.n_pad)))
         return cudaErrorInvalidValue;
     const int64_t tiles = (n_tokens + R_BM - 1) / R_BM;
-    // K split: the largest power of two S <= R_MAX_SPLIT with tiles x S
-    // within the SM count, at most one CTA per 64-wide K block, and a
-    // shared-memory layout that fits
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return cudaErrorNoDevice;
     const int smem_max = optin < R_SMEM_MAX ? optin : R_SMEM_MAX;
-    auto layout_for = [&](int64_t sp, RouterLayout* L) {
+    auto layout_for = [&](int64_t sp, bool pair, RouterLayout* L) {
         const int kb = static_cast<int>((p.k_blocks + sp - 1) / sp);
-        return router_layout(p.n_pad, static_cast<int>(sp), kb, smem_max, L);
+        return router_layout(p.n_pad, static_cast<int>(sp), pair, kb, smem_max, L);
     };
+    // K split: the largest power of two S <= R_MAX_SPLIT with tiles x S
+    // within the SM count, at most one CTA per 64-wide K block, and a
+    // shared-memory layout that fits
     RouterLayout L{};
     int64_t split = 1;
     while (split * 2 <= R_MAX_SPLIT && tiles * split * 2 <= device_sm_count() && split * 2 <= p.k_blocks &&
-           layout_for(split * 2, &L))
+           layout_for(split * 2, false, &L))
         split *= 2;
     const int kmax = top_k <= 4 ? 4 : top_k <= 8 ? 8 : 16;
-    auto kernel_for = [kmax](int64_t sp) {
+    auto kernel_for = [kmax](int64_t sp, bool pair) {
+        if (pair) return kmax == 4 ? router_kernel<1, 4, true> : kmax == 8 ? router_kernel<1, 8, true>
+                                                                             : router_kernel<1, 16, true>;
         if (kmax == 4)
-            return sp >= 8 ? router_kernel<8, 4> : sp == 4 ? router_kernel<4, 4> : sp == 2 ? router_kernel<2, 4>
-                                                                                          : router_kernel<1, 4>;
+            return sp >= 8 ? router_kernel<8, 4, false> : sp == 4 ? router_kernel<4, 4, false>
+                 : sp == 2 ? router_kernel<2, 4, false> : router_kernel<1, 4, false>;
         if (kmax == 8)
-            return sp >= 8 ? router_kernel<8, 8> : sp == 4 ? router_kernel<4, 8> : sp == 2 ? router_kernel<2, 8>
-                                                                                          : router_kernel<1, 8>;
-        return sp >= 8 ? router_kernel<8, 16> : sp == 4 ? router_kernel<4, 16> : sp == 2 ? router_kernel<2, 16>
-                                                                                        : router_kernel<1, 16>;
+            return sp >= 8 ? router_kernel<8, 8, false> : sp == 4 ? router_kernel<4, 8, false>
+                 : sp == 2 ? router_kernel<2, 8, false> : router_kernel<1, 8, false>;
+        return sp >= 8 ? router_kernel<8, 16, false> : sp == 4 ? router_kernel<4, 16, false>
+             : sp == 2 ? router_kernel<2, 16, false> : router_kernel<1, 16, false>;
     };
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -680,43 +726,65 @@ cudaError_t launch_router(const uint16_t* x, int64_t n_tokens, int32_t hidden, c
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // a cluster size the device can place (clusters live inside one GPC);
+    // a cluster shape the device can place (clusters live inside one GPC);
     // the answer is cached per device, kernel and shared-memory size
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int64_t, size_t>, bool> placeable;
-    for (; split >= 1; split /= 2) {
-        if (!layout_for(split, &L)) {
-            if (split == 1) return cudaErrorInvalidConfiguration;
-            continue;
-        }
+    static std::map<std::tuple<int, int, int64_t, bool, size_t>, bool> placeable;
+    auto placeable_for = [&](int64_t sp, bool pair) -> int {   // 1 yes, 0 no, -1 error
+        const int64_t cl = pair ? 2 : sp;
         std::lock_guard<std::mutex> lock(mu);
-        const auto key = std::make_tuple(dev, kmax, split, L.smem);
+        const auto key = std::make_tuple(dev, kmax, sp, pair, L.smem);
         auto it = placeable.find(key);
         if (it == placeable.end()) {
-            cudaError_t e = cudaFuncSetAttribute(kernel_for(split), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 smem_max);
-            if (e != cudaSuccess) return e;
-            attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-            cfg.gridDim = dim3(static_cast<unsigned>(split));
+            if (cudaFuncSetAttribute(kernel_for(sp, pair), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
+                cudaSuccess)
+                return -1;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+            cfg.gridDim = dim3(static_cast<unsigned>(cl));
             cfg.dynamicSmemBytes = L.smem;
             int n = 0;
-            const bool ok = split == 1 || (cudaOccupancyMaxActiveClusters(&n, kernel_for(split), &cfg) == cudaSuccess &&
-                                           n > 0);
+            const bool ok = cl == 1 || (cudaOccupancyMaxActiveClusters(&n, kernel_for(sp, pair), &cfg) == cudaSuccess &&
+                                        n > 0);
             if (!ok) cudaGetLastError();
             it = placeable.emplace(key, ok).first;
         }
-        if (it->second) break;
+        return it->second ? 1 : 0;
+    };
+    // Without a K split (as many tiles as SMs, or more), tiles pair up on
+    // 2-SM MMAs that split W_g's rows when that moves fewer bytes per SM
+    // (at least 64 experts' rows)
+    bool pair = false;
+    for (; split >= 1; split /= 2) {
+        if (!layout_for(split, false, &L)) {
+            if (split == 1) return cudaErrorInvalidConfiguration;
+            continue;
+        }
+        const int r = placeable_for(split, false);
+        if (r < 0) return cudaErrorInvalidConfiguration;
+        if (r == 1) break;
     }
+    if (split == 1 && tiles >= 2 && p.n_pad >= 64) {
+        RouterLayout L1 = L;
+        if (layout_for(1, true, &L)) {
+            const int r = placeable_for(1, true);
+            if (r < 0) return cudaErrorInvalidConfiguration;
+            pair = r == 1;
+        }
+        if (!pair) L = L1;
+    }
+    if (pair && !router_map(&map_w, router_w, static_cast<uint64_t>(n_experts), static_cast<uint64_t>(hidden),
+                            static_cast<uint32_t>(p.n_pad / 2)))
+        return cudaErrorInvalidValue;
     p.stages = L.stages;
     p.stage_bytes = L.stage_bytes;
     p.rs = L.rs;
     p.off_slots = L.off_slots;
     p.off_cand = L.off_cand;
     p.off_bars = L.off_bars;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
+    attr[0].val.clusterDim.x = static_cast<unsigned>(pair ? 2 : split);
+    cfg.gridDim = dim3(static_cast<unsigned>(pair ? (tiles + 1) / 2 * 2 : tiles * split));
     cfg.dynamicSmemBytes = L.smem;
-    return cudaLaunchKernelEx(&cfg, kernel_for(split), map_x, map_w, p);
+    return cudaLaunchKernelEx(&cfg, kernel_for(split, pair), map_x, map_w, p);
 }
 
 }  // namespace moe

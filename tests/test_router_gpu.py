@@ -53,7 +53,7 @@ def _check(x, wg, k):
 
 
 @pytest.mark.parametrize("name,tokens", [("tiny", None), ("dsv2_lite", None), ("decode_skewed", None),
-                                         ("mixtral", 1000), ("dsv3", 1000)])
+                                         ("mixtral", 1000), ("dsv3", 1000), ("dsv3", None)])
 def test_router_workloads(name, tokens):
     w = workloads.WORKLOADS[name]
     T = tokens or w.tokens
@@ -92,6 +92,8 @@ def _exact_case(T, E, H, seed, zero_w=False):
 @pytest.mark.parametrize("T,E,k,H,zero_w", [
     (300, 64, 6, 128, False), (200, 256, 8, 256, False), (130, 16, 16, 128, False), (64, 40, 5, 128, False),
     (33, 128, 8, 2048, False),                       # one ragged tile, the hidden split over the cluster
+    (9800, 64, 6, 128, False), (9800, 256, 8, 256, False),   # more tiles than half the SMs: 2-SM pairs, a spare CTA
+    (9800, 256, 8, 128, True),
     (100, 64, 6, 128, True), (100, 256, 8, 128, True), (100, 16, 4, 128, True), (20, 128, 8, 1024, True)])
 def test_router_exact_ties(T, E, k, H, zero_w):
     x, wg = _exact_case(T, E, H, seed=T + E, zero_w=zero_w)
@@ -103,3 +105,13 @@ def test_router_exact_ties(T, E, k, H, zero_w):
     assert np.allclose(w_g, w_o, rtol=2e-5, atol=1e-8)
     if zero_w:
         assert np.array_equal(ids_g, np.broadcast_to(np.arange(k, dtype=np.int32), (T, k)))
+
+
+@pytest.mark.parametrize("T,E,k,H", [(10000, 256, 8, 512), (19000, 96, 4, 256)])
+def test_router_pairs(T, E, k, H):
+    """Token counts whose tiles outnumber half the SMs: no K split, tiles paired
+    on 2-SM MMAs that split W_g's rows (odd tile counts leave a spare CTA)."""
+    w = small_workload(tokens=T, top_k=k, experts=E, hidden=H, intermediate=128)
+    x = workloads.tokens(w, seed=T)
+    wg = workloads.router_weights(w, seed=T)
+    _check(x, wg, k)
