@@ -4,7 +4,9 @@
 // padding_M with padding_M = block_token).
 //
 // One CTA of 1024 threads: the counts of up to MOE_MAX_EXPERTS experts live in
-// shared memory, the scans are warp-shuffle scans over one expert per thread,
+// shared memory (for at most 256 experts one histogram per warp, summed
+// afterwards, so that a popular expert's increments do not all queue on one
+// address), the scans are warp-shuffle scans over one expert per thread,
 // and each block finds its expert by binary search over the padded offsets
 // (the page scans linearly; both give the last expert whose padded start is
 // <= bx * block_token).  No workspace and no host synchronisation: the tables
@@ -21,6 +23,7 @@ namespace moe {
 namespace {
 
 constexpr int DISPATCH_THREADS = 1024;
+constexpr int PRIV_EXPERTS = 256;   // per-warp histograms up to this many experts
 
 __device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
 #pragma unroll
@@ -40,6 +43,7 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     __shared__ int32_t pad_s[MOE_MAX_EXPERTS + 1];
     __shared__ int32_t wsum_c[DISPATCH_THREADS / 32];
     __shared__ int32_t wsum_p[DISPATCH_THREADS / 32];
+    __shared__ int32_t hist_w[DISPATCH_THREADS / 32][PRIV_EXPERTS];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // A forward launched right behind this kernel may start its own set-up
@@ -51,7 +55,13 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     // router that writes topk_ids).  Only the shared-memory set-up overlaps
     // that kernel: griddepcontrol.wait is the one point after which its
     // writes are visible, so every global read and write comes after it.
-    for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
+    const bool priv = n_experts <= PRIV_EXPERTS;
+    if (priv) {
+        for (int i = tid; i < (DISPATCH_THREADS / 32) * PRIV_EXPERTS; i += DISPATCH_THREADS)
+            (&hist_w[0][0])[i] = 0;
+    } else {
+        for (int e = tid; e < n_experts; e += DISPATCH_THREADS) cnt[e] = 0;
+    }
     pdl_wait_prior_grid();
     __syncthreads();
 
@@ -59,8 +69,9 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     // in flight before their atomics, so a few memory round trips cover the
     // whole input; a scalar loop takes the unaligned case and the tail
     bool bad = false;
+    int32_t* hist = priv ? hist_w[warp] : cnt;
     auto count = [&](int32_t v) {
-        if (static_cast<uint32_t>(v) < static_cast<uint32_t>(n_experts)) atomicAdd(&cnt[v], 1);
+        if (static_cast<uint32_t>(v) < static_cast<uint32_t>(n_experts)) atomicAdd(&hist[v], 1);
         else bad = true;
     };
     int64_t done = 0;
@@ -90,6 +101,15 @@ build_dispatch_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32
     for (int64_t f = done + tid; f < pairs; f += DISPATCH_THREADS) count(__ldg(topk_ids + f));
     if (bad && status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
+    if (priv) {
+        for (int e = tid; e < n_experts; e += DISPATCH_THREADS) {
+            int32_t sum = 0;
+#pragma unroll 8
+            for (int w = 0; w < DISPATCH_THREADS / 32; ++w) sum += hist_w[w][e];
+            cnt[e] = sum;
+        }
+        __syncthreads();
+    }
 
     // exclusive scans of the counts (compact offsets) and of the padded steps
     const int e = tid;                                  // n_experts <= 1024 threads
