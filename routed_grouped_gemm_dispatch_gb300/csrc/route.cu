@@ -20,6 +20,9 @@
 //      pair's padded row, its routed weight at the compact index, and copies
 //      the token's activation row (one warp per pair, 16-byte vectors).
 // Combine: one CTA per token, fp32 sum over j = 0..k-1 in order, one rounding.
+// Every launch here uses programmatic dependent launch: a kernel may start
+// during the tail of the previous one on the stream, and waits for it
+// (griddepcontrol.wait) before its first global access.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -27,6 +30,7 @@
 
 #include "../../include/moe_gb300.h"
 #include "moe_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -42,8 +46,12 @@ rank_chunks_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32_t 
     int32_t* running = sh;                                    // [E] pairs of e seen so far in the chunk
     uint8_t* wcnt = reinterpret_cast<uint8_t*>(sh + n_experts);   // [RANK_WARPS][E] per-warp counts
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // launched with programmatic dependent launch: the shared-memory set-up
+    // may overlap the previous kernel; global reads come after its completion
+    pdl_launch_dependents();
     for (int e = tid; e < n_experts; e += RANK_THREADS) running[e] = 0;
     for (int i = tid; i < RANK_WARPS * n_experts; i += RANK_THREADS) wcnt[i] = 0;
+    pdl_wait_prior_grid();
     __syncthreads();
     const int64_t chunk0 = static_cast<int64_t>(blockIdx.x) * PACK_CHUNK;
     bool bad = false;
@@ -87,6 +95,8 @@ rank_chunks_kernel(const int32_t* __restrict__ topk_ids, int64_t pairs, int32_t 
 __global__ void scan_chunks_kernel(int32_t* chunk_hist, int32_t n_chunks, int32_t n_experts) {
     const int32_t e = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait_prior_grid();
     if (e >= n_experts) return;
     int32_t carry = 0;
     for (int32_t c0 = 0; c0 < n_chunks; c0 += 32) {
@@ -114,6 +124,8 @@ __global__ void place_pairs_kernel(const int32_t* __restrict__ topk_ids, const f
                                    float* __restrict__ rw_compact, int32_t* __restrict__ pair_rows, int32_t* status) {
     const int64_t f = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait_prior_grid();
     if (f >= pairs) return;
     const int32_t e = __ldg(topk_ids + f);
     if (static_cast<uint32_t>(e) >= static_cast<uint32_t>(n_experts)) {
@@ -168,6 +180,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
 combine_kernel(const uint16_t* __restrict__ out, int64_t rows_total, int32_t hidden,
                const int32_t* __restrict__ pair_rows, int32_t top_k, uint16_t* __restrict__ y) {
     const int64_t t = blockIdx.x;
+    pdl_launch_dependents();
+    pdl_wait_prior_grid();
     for (int32_t c8 = threadIdx.x; c8 < hidden / 8; c8 += COMBINE_THREADS) {
         float acc[8];
 #pragma unroll
@@ -202,6 +216,25 @@ combine_kernel(const uint16_t* __restrict__ out, int64_t rows_total, int32_t hid
     }
 }
 
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous kernel on the stream finishes; every kernel here waits for it
+// (griddepcontrol.wait) before its first global access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
 
 int64_t pack_workspace_bytes(int64_t pairs, int32_t n_experts) {
@@ -224,28 +257,25 @@ cudaError_t launch_pack(const int32_t* topk_ids, const float* topk_weights, int6
     cudaError_t err = cudaFuncSetAttribute(rank_chunks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    rank_chunks_kernel<<<chunks, RANK_THREADS, smem, stream>>>(topk_ids, pairs, n_experts, local_rank, hist,
-                                                               status);
-    scan_chunks_kernel<<<(n_experts + 7) / 8, 256, 0, stream>>>(hist, chunks, n_experts);
+    if ((err = launch_pdl(rank_chunks_kernel, dim3(chunks), dim3(RANK_THREADS), smem, stream, topk_ids, pairs,
+                          n_experts, local_rank, hist, status)) != cudaSuccess)
+        return err;
+    if ((err = launch_pdl(scan_chunks_kernel, dim3((n_experts + 7) / 8), dim3(256), 0, stream, hist, chunks,
+                          n_experts)) != cudaSuccess)
+        return err;
     const int64_t warps = pairs;
     const int64_t blocks = (warps * 32 + 255) / 256;
-    place_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        topk_ids, topk_weights, pairs, top_k, n_experts, local_rank, hist, offsets, padded, x_tokens, hidden,
-        rows_total, valid_total, x_packed, rw_compact, pair_rows, status);
-    return cudaGetLastError();
+    return launch_pdl(place_pairs_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, topk_ids,
+                      topk_weights, pairs, top_k, n_experts, local_rank, hist, offsets, padded, x_tokens, hidden,
+                      rows_total, valid_total, x_packed, rw_compact, pair_rows, status);
 }
 
 cudaError_t launch_combine(const uint16_t* out, int64_t rows_total, int32_t hidden, const int32_t* pair_rows,
                            int64_t n_tokens, int32_t top_k, uint16_t* y, cudaStream_t stream) {
     if (n_tokens == 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>(n_tokens);
-    if (top_k <= 2)
-        combine_kernel<2><<<grid, COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden, pair_rows, top_k, y);
-    else if (top_k <= 4)
-        combine_kernel<4><<<grid, COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden, pair_rows, top_k, y);
-    else
-        combine_kernel<8><<<grid, COMBINE_THREADS, 0, stream>>>(out, rows_total, hidden, pair_rows, top_k, y);
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>(n_tokens));
+    auto kernel = top_k <= 2 ? combine_kernel<2> : top_k <= 4 ? combine_kernel<4> : combine_kernel<8>;
+    return launch_pdl(kernel, grid, dim3(COMBINE_THREADS), 0, stream, out, rows_total, hidden, pair_rows, top_k, y);
 }
 
 }  // namespace moe
