@@ -69,6 +69,9 @@ def build(force: bool = False, debug: bool = False) -> str:
 def lib():
     """The loaded C library; raises if it has not been built."""
     global _lib
+    L = _lib
+    if L is not None:
+        return L
     with _lock:
         if _lib is not None:
             return _lib
@@ -125,6 +128,11 @@ def num_blocks(pairs: int, n_experts: int, block_token: int = BLOCK_TOKEN) -> in
 def _stream(stream):
     import torch
     if stream is None:
+        # the current stream's handle without building a Stream object (the
+        # call Triton uses too); the public query where it does not exist
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     return getattr(stream, "cuda_stream", stream)
 
@@ -135,6 +143,10 @@ def _ptr(t):
 
 def _dev(t, name, dtype, ndim=None):
     import torch
+    # the common case in one expression; the checks below name what is wrong
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype is dtype and (ndim is None or t.dim() == ndim)
+            and t.is_contiguous()):
+        return t
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device.type != "cuda":
