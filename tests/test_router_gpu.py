@@ -107,7 +107,7 @@ def test_router_exact_ties(T, E, k, H, zero_w):
         assert np.array_equal(ids_g, np.broadcast_to(np.arange(k, dtype=np.int32), (T, k)))
 
 
-@pytest.mark.parametrize("T,E,k,H", [(10000, 256, 8, 512), (19000, 96, 4, 256)])
+@pytest.mark.parametrize("T,E,k,H", [(10000, 256, 8, 512), (19000, 96, 4, 256), (19000, 200, 16, 128)])
 def test_router_pairs(T, E, k, H):
     """Token counts whose tiles outnumber half the SMs: no K split, tiles paired
     on 2-SM MMAs that split W_g's rows (odd tile counts leave a spare CTA)."""
